@@ -1,0 +1,410 @@
+#!/usr/bin/env python
+"""Benchmark of the per-rank LAGA compute on GB300.
+
+One step = the whole hot path on one batch: laga_fwd (latent LayerNorm,
+RoPE, head-shard up-projection, causal attention forward) followed by
+laga_bwd (attention backward, up-projection backward, LayerNorm/RoPE
+backward) of a 16-head DeepSeek-V3-dim shard at S=16384 (bf16 operands,
+fp32 accumulation).  Inputs are seeded synthetic tensors of the workload's
+shapes and distributions.
+
+value = attention fwd+bwd algorithmic FLOPs (H*S^2*1152, causal S^2/2
+pairs) / the full step time, in TFLOP/s; the step time includes the
+up-projection and the norm kernels, so value under-states the attention
+kernels' own rate (reported separately as attn_kernels_tflops).
+
+Usage:  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun each rank computes its own head shard of an N*16-head layer
+(no collective on the data path: weak scaling); rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LAGA attn fwd+bwd TFLOP/s (V3 dims, 16-head shard, S=16K); % of BF16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, help="workload configuration (default 2)")
+    ap.add_argument("--form", default="laga", choices=["laga", "explicit"])
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["bf16_tflops"]), float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, FALLBACK_HBM_GBS, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="laga_clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["-i", self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"),
+                                         stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": num(rows[0][2]), "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows), "reasons": reasons}
+
+
+# ----------------------------------------------------------------- ncu traffic
+def ncu_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes of one kernel from its committed ncu summary, if
+    the summary was taken on the current kernel source (same sha256)."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    src = re.search(r"source_sha256:\s*([0-9a-f]+)\s+(\S+)", txt)
+    if not m or not src:
+        return None
+    f = os.path.join(ROOT, src.group(2))
+    if not os.path.exists(f) or hashlib.sha256(open(f, "rb").read()).hexdigest() != src.group(1):
+        return None
+    return float(m.group(1))
+
+
+# ----------------------------------------------------------------- kernels' work
+def kernel_work(name: str, S: int, H: int, B: int = 1):
+    """(bound, algorithmic units per launch) of each library kernel: FLOPs
+    for tensor-core work, DRAM bytes for the HBM-bound kernels."""
+    pairs = B * H * S * S / 2.0
+    T, R = B * S, B * S * H
+    table = {
+        "attn_fwd": ("tensor", pairs * (2 * 192 + 2 * 128)),
+        "attn_bwd": ("tensor", pairs * (6 * 192 + 4 * 128)),
+        "attn_bwd_dkdv": ("tensor", pairs * (2 * 192 + 2 * 128 + 2 * 128 + 2 * 192)),
+        "attn_bwd_dq": ("tensor", pairs * 2 * 192),
+        "upproj": ("tensor", 2.0 * T * 512 * H * 256),
+        "upproj_dw": ("tensor", 2.0 * T * 512 * H * 256),
+        "upproj_dl": ("tensor", 2.0 * T * 512 * H * 256),
+        # HBM-bound: bytes read + written once
+        "prep_fwd": ("hbm", T * 576 * 2 + R * 64 * 2 + T * (512 * 2 + 8 + 64 * 2) + R * 64 * 2),
+        "bwd_pre": ("hbm", 2 * R * 128 * 2 + R * 4),
+        "dq_final": ("hbm", R * 192 * 4 + R * 192 * 2),
+        "norm_bwd": ("hbm", T * 512 * 4 + T * 576 * 2 + T * 8 + R * 64 * 4 + T * 576 * 4),
+    }
+    return table.get(name, ("hbm", None))
+
+
+def attention_flops(S, H, B=1):
+    pairs = B * H * S * S / 2.0
+    return pairs * (2 * 192 + 2 * 128), pairs * (6 * 192 + 4 * 128)
+
+
+# ----------------------------------------------------------------- CPU oracle
+def oracle_sample(wl, S_sample: int, head: int = 0):
+    """Time the fp64 oracle's fwd+bwd of one head of the workload on the
+    first S_sample tokens; returns (seconds, attention FLOPs of the sample)."""
+    import dataclasses
+    import oracle
+    from laga_inputs import as_f64, make_inputs
+    sub = dataclasses.replace(wl, S=S_sample, H=1, n_h_total=1, head_offset=0)
+    cpu = make_inputs(sub)
+    a = {k: as_f64(v) for k, v in cpu.items()}
+    d = oracle.Dims(S=sub.S, H=1)
+    t0 = time.perf_counter()
+    _, _, st = oracle.forward(a["q"], a["c"], a["w"], a["gamma"], a["cos"], a["sin"], d)
+    oracle.backward(st, a["dO"])
+    dt = time.perf_counter() - t0
+    f, b = attention_flops(S_sample, 1)
+    return dt, f + b
+
+
+def run_reference(args, rank):
+    from laga_inputs import config
+    if rank != 0:
+        return
+    wl = config(args.config)
+    S_sample = min(wl.S, 8192)
+    times, flops = [], 0.0
+    for i in range(args.warmup + args.steps):
+        dt, flops = oracle_sample(wl, S_sample)
+        if i >= args.warmup:
+            times.append(dt)
+    sec = sum(times) / len(times)
+    value = flops / sec / 1e12
+    sample = (f"fp64 NumPy oracle fwd+bwd of 1 head on the first {S_sample} tokens of the "
+              f"{wl.name} workload per step")
+    cores = os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "S": wl.S, "H": wl.H, "sample_S": S_sample,
+                       "sample_heads": 1},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import dataclasses
+    import torch
+    import torch.distributed as dist
+    import sequence_latent_norm_gb300 as pkg
+    from laga_inputs import config, make_inputs
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    base = config(args.config)
+    # each rank computes its own head shard of a world*H-head layer
+    wl = dataclasses.replace(base, n_h_total=base.H * world, head_offset=base.H * rank)
+    S, H, B = wl.S, wl.H, wl.B
+
+    # CPU baseline first (rank 0, one GPU only): the oracle as it stands.
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        dt, fl = oracle_sample(base, base.S)
+        cpu_baseline = {"value": fl / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(),
+                        "kind": "oracle",
+                        "sample": f"fp64 NumPy oracle fwd+bwd of 1 of the {H} heads over all "
+                                  f"{S} tokens ({dt:.1f} s)"}
+
+    cpu = make_inputs(wl)
+    t = {k: v.to(dev) for k, v in cpu.items()}
+    shard = pkg.Shard(S=S, H=H, n_h_total=wl.n_h_total, head_offset=wl.head_offset, B=B,
+                      io_dtype=wl.dtype, form=args.form)
+    run = pkg.Laga(shard, device=dev)
+    _ = run.ws_bwd
+    f32 = torch.float32
+    o = torch.empty(B, S, H, 128, dtype=torch.bfloat16, device=dev)
+    lse = torch.empty(B, H, S, dtype=f32, device=dev)
+    dq = torch.empty(B, S, H, 192, dtype=torch.bfloat16, device=dev)
+    dc = torch.empty(B, S, 576, dtype=f32, device=dev)
+    dw = torch.empty(512, H * 256, dtype=f32, device=dev)
+    dg = torch.empty(512, dtype=f32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    launches = [0]
+
+    def step(tt):
+        run.forward(tt["q"], tt["c"], tt["w"], tt["gamma"], tt["cos"], tt["sin"], o, lse)
+        n = pkg._lib.last_launch_count()
+        run.backward(tt["q"], tt["c"], tt["w"], tt["gamma"], tt["cos"], tt["sin"], o, lse,
+                     tt["dO"], dq, dc, dw, dg)
+        launches[0] = n + pkg._lib.last_launch_count()
+
+    for _ in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize(dev)
+    pkg._lib.sync_check()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    gpu_id = None
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = None
+    clocks = ClockSampler(gpu_id)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    pkg._lib.profile_reset()
+    pkg._lib.profile_enable(True)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flush, outside the timed events
+        ev[i][0].record(stream)
+        step(t)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    pkg._lib.profile_enable(False)
+    prof = pkg._lib.profile_read()
+    pkg._lib.sync_check()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = sum(step_ms)
+    if world > 1:
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    fwd_f, bwd_f = attention_flops(S, H, B)
+    attn_flops = fwd_f + bwd_f
+    value = world * attn_flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end through the public API with host buffers
+    host_in = {k: v.pin_memory() for k, v in cpu.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    outs = [o, lse, dq, dc, dw, dg]
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    d2h = sum(x.numel() * x.element_size() for x in outs)
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in cpu.items()}
+    e2e_ms = []
+    for i in range(args.e2e_steps + 1):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        step(dev_in)
+        for x, hx in zip(outs, host_out):
+            hx.copy_(x, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        if i > 0:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = world * attn_flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+
+    # ---- per-kernel rates and the roofline of the dominant kernel
+    peak_tf, peak_gbs, peak_src = measured_peaks()
+    kernels = {}
+    for name, (ms, n) in prof.items():
+        bound, units = kernel_work(name, S, H, B)
+        per = ms / n
+        ent = {"launches_per_step": n / args.steps, "ms_per_launch": round(per, 4),
+               "share": round(ms / sum(v[0] for v in prof.values()), 4)}
+        if units is not None:
+            rate = units / (per * 1e-3)
+            ent["achieved"] = round(rate / 1e12 if bound == "tensor" else rate / 1e9, 2)
+            ent["unit"] = "TFLOP/s" if bound == "tensor" else "GB/s"
+        kernels[name] = ent
+    top = max(prof.items(), key=lambda kv: kv[1][0])[0]
+    bound, units = kernel_work(top, S, H, B)
+    per_ms = prof[top][0] / prof[top][1]
+    if bound == "tensor":
+        ach = units / (per_ms * 1e-3) / 1e12
+        roof = {"kernel": top, "bound": "tensor", "achieved": round(ach, 2), "peak": peak_tf,
+                "unit": "TFLOP/s", "frac": round(ach / peak_tf, 4),
+                "peak_source": f"{peak_src} bf16 dense (burst)"}
+    else:
+        ach = units / (per_ms * 1e-3) / 1e9
+        roof = {"kernel": top, "bound": "hbm", "achieved": round(ach, 1), "peak": peak_gbs,
+                "unit": "GB/s", "frac": round(ach / peak_gbs, 4),
+                "peak_source": f"{peak_src} HBM copy"}
+    roof["traffic"] = ncu_traffic(top, base.name)
+    attn_ms = sum(prof[k][0] for k in prof if k.startswith("attn")) / args.steps
+    up_f = 3 * 2.0 * B * S * 512 * H * 256
+    line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": base.name, "B": B, "S": S, "H": H, "n_h_total": wl.n_h_total,
+                       "d_nope": 128, "d_rope": 64, "d_v": 128, "d_kv": 512, "form": args.form,
+                       "parallelism": f"{world} independent head shards (no data-path collective)",
+                       "l2": "flushed between steps by a 512 MB write outside the timed events",
+                       "value_definition": "H*S^2*1152 attention FLOPs / full hot-path step time"},
+            "pct_of_bf16_peak": round(100 * value / world / peak_tf, 2),
+            "attn_kernels_tflops": round(attn_flops / (attn_ms * 1e-3) / 1e12, 2),
+            "block_tflops": round((attn_flops + up_f) / (ms_per_step * 1e-3) / 1e12, 2),
+            "wall_s_timed": round(t_wall, 3),
+            "clocks": clk,
+            "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 3)},
+            "gpu_launches": launches[0] * args.steps,
+            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu_baseline}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

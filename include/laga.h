@@ -1,0 +1,168 @@
+/*
+ * laga.h -- C ABI of the GB300 (sm_103a) per-rank LAGA compute.
+ *
+ * LAGA (Latent All-Gather Attention), from "A Training-Memory Regression in
+ * MLA Sequence Parallelism: Why Megatron-Core Forbids Absorption, and LAGA --
+ * a Communication-Efficient Fix" (arXiv 2607.17644v1).  After the latent
+ * all-gather (Algorithm 1 step 3) each rank holds the full-sequence latent
+ * c = [latent (d_kv) | k_pe (d_rope)] and its head shard of q.  This library
+ * runs the rest of the rank's attention on one GPU:
+ *
+ *   a1  L = LayerNorm(latent) * gamma           (Section 2.1, Alg. 1 step 1)
+ *   a2  RoPE of k_pe (shared by all heads) and of q_rope   (Section 5.3)
+ *   a3  KV = L . W_kv_b[:, shard]  -> k_nope | v per head  (Alg. 1 step 4,
+ *                                                          Section 5.1 eq.)
+ *   a4  causal attention, scores = (q_nope||q_rope)(k_nope||k_pe)^T/sqrt(d),
+ *       out = softmax(scores) v                        (Alg. 1 step 5)
+ *   a5-a7 the backward of all of the above: dq, dc, dW_kv_b shard, dgamma
+ *       (Section 5.2)
+ *
+ * Conventions (the page leaves these open; each is the plainest reading):
+ *   - d = d_nope + d_rope; causal means key j is visible to query i iff j<=i.
+ *   - LayerNorm: biased variance, gain gamma, no bias, eps = ln_eps.
+ *   - RoPE rotates pairs (i, i + d_rope/2) by the angle whose cos/sin the
+ *     caller passes in cos/sin [S, d_rope/2] (fp32, positions 0..S-1 of the
+ *     gathered sequence).  q is passed raw; the library rotates q_rope and
+ *     k_pe itself; dq and dc are gradients with respect to the raw inputs.
+ *   - W_kv_b is [d_kv, n_h_total * (d_nope + d_v)] row-major; the columns of
+ *     head i are [k_nope (d_nope) | v (d_v)]; this call's shard is heads
+ *     [head_offset, head_offset + n_h_shard).
+ *
+ * Ownership and execution.  The caller allocates every buffer (device
+ * memory unless stated otherwise).  The library never allocates, frees or
+ * synchronises (except laga_sync_check); every call only validates its
+ * arguments on the host and enqueues kernels on `stream` (a cudaStream_t
+ * passed as void*, NULL = legacy default stream).  Outputs are overwritten,
+ * not accumulated.  Summing the partial dc and dgamma of several head shards
+ * is the caller's job (the reduce-scatter / all-reduce of Section 5.2).
+ *
+ * Errors.  All argument, size and alignment checks happen before the first
+ * launch; on any error nothing is enqueued.  Device pointers must be 16-byte
+ * aligned.  A launch failure returns LAGA_ERR_CUDA.  Device-side waits are
+ * bounded; one that gives up records LAGA_ERR_TIMEOUT in a device flag that
+ * laga_sync_check() (or the next laga_fwd/laga_bwd on the same device)
+ * reports.  No C++ exception crosses this ABI.
+ */
+#ifndef LAGA_H
+#define LAGA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LAGA_OK = 0,
+  LAGA_ERR_ARG = 1,          /* bad size, NULL pointer, unknown enum value   */
+  LAGA_ERR_ALIGN = 2,        /* a pointer is not 16-byte aligned             */
+  LAGA_ERR_WORKSPACE = 3,    /* workspace smaller than laga_workspace_bytes  */
+  LAGA_ERR_UNSUPPORTED = 4,  /* valid but not built: e.g. causal = 0        */
+  LAGA_ERR_CUDA = 5,         /* a CUDA runtime/driver call failed            */
+  LAGA_ERR_TIMEOUT = 6       /* a bounded device wait gave up                */
+} laga_status;
+
+/* Which of the three forms of Section 3 to run on one rank.
+ *  LAGA      latent gathered, K/V rebuilt per head shard, K/V layout
+ *            [B, S, H, d_nope + d_v] (token-major).
+ *  EXPLICIT  same arithmetic, K/V in the head-major layout [B, H, S, ...]
+ *            that the explicit form's all-to-all produces (Section 3.2, B1);
+ *            at SP = 1 results are bit-identical to LAGA (Proposition 1).
+ *  ABSORBED  q_absorbed = W^k^T q_nope, attention over the latent, latent
+ *            accumulator, V up-projection afterwards (Section 3.2, B2); the
+ *            memory-trap contrast path, not a performance path. */
+typedef enum { LAGA_FORM_LAGA = 0, LAGA_FORM_EXPLICIT = 1, LAGA_FORM_ABSORBED = 2 } laga_form;
+
+/* Element type of q, c, W_kv_b, O, dO and dq.  Compute is bf16 operands with
+ * fp32 accumulation in both cases; fp32 I/O is rounded to bf16 on-device. */
+typedef enum { LAGA_BF16 = 0, LAGA_FP32 = 1 } laga_dtype;
+
+typedef struct {
+  int B;            /* batch, >= 1                                            */
+  int S;            /* full (gathered) sequence length, >= 1                  */
+  int n_h_total;    /* heads whose columns W_kv_b holds                        */
+  int head_offset;  /* first head of this shard                                */
+  int n_h_shard;    /* heads in this shard (n_h / SP); offset+shard <= total   */
+  int d_nope;       /* multiples of 16; d_nope, d_v <= 128, d_rope <= 64 even, */
+  int d_rope;       /* d_kv <= 512.  DeepSeek-V3: 128 / 64 / 128 / 512.        */
+  int d_v;
+  int d_kv;
+  float scale;      /* softmax scale; 0 selects 1/sqrt(d_nope + d_rope)        */
+  float ln_eps;     /* LayerNorm epsilon (1e-5 in the workloads)               */
+  int causal;       /* must be 1                                               */
+  laga_dtype io_dtype;
+  laga_form form;
+} laga_dims;
+
+/* Workspace passes. */
+#define LAGA_WS_SAVED 0   /* written by laga_fwd, read by laga_bwd: keep it    */
+#define LAGA_WS_BWD 1     /* transient scratch of laga_bwd                     */
+
+/* Bytes of workspace `pass` needs for these dims (0 if the dims are
+ * invalid).  Host-only, no CUDA call. */
+size_t laga_workspace_bytes(const laga_dims* dims, int pass);
+
+/* Enumerate the named tensors inside workspace `pass` (activation
+ * accounting).  index runs from 0; returns LAGA_ERR_ARG past the last one.
+ * *name is a static string, *offset/*bytes are byte offsets inside the
+ * workspace.  Host-only. */
+laga_status laga_workspace_tensor(const laga_dims* dims, int pass, int index,
+                                  const char** name, size_t* offset, size_t* bytes);
+
+/* Forward, steps a1-a4.
+ *   q      [B, S, n_h_shard, d_nope + d_rope]  io dtype, raw (un-rotated)
+ *   c      [B, S, d_kv + d_rope]                io dtype, [latent | k_pe]
+ *   w_kvb  [d_kv, n_h_total * (d_nope + d_v)]   io dtype, full matrix
+ *   gamma  [d_kv] fp32;  cos, sin [S, d_rope/2] fp32
+ *   o      [B, S, n_h_shard, d_v]               io dtype (output)
+ *   lse    [B, n_h_shard, S] fp32 natural-log row log-sum-exp (output)
+ *   ws_saved / saved_bytes: LAGA_WS_SAVED workspace; must stay unchanged
+ *          until the matching laga_bwd. */
+laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
+                     const float* gamma, const float* cos, const float* sin,
+                     void* o, float* lse, void* ws_saved, size_t saved_bytes, void* stream);
+
+/* Backward, steps a5-a7, for the loss sum(O * dO).
+ *   q, c, w_kvb, gamma, cos, sin, o, lse: exactly as given to / returned by
+ *          the matching laga_fwd;  d_o [B, S, n_h_shard, d_v] io dtype
+ *   dq     [B, S, n_h_shard, d_nope + d_rope]   io dtype (output)
+ *   dc     [B, S, d_kv + d_rope] fp32: this shard's partial (output)
+ *   dw     [d_kv, n_h_shard * (d_nope + d_v)] fp32: gradient of this
+ *          shard's columns of W_kv_b (output)
+ *   dgamma [d_kv] fp32: this shard's partial (output)
+ *   ws_saved: the forward's saved workspace (read only)
+ *   ws_bwd / bwd_bytes: LAGA_WS_BWD scratch. */
+laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
+                     const float* gamma, const float* cos, const float* sin,
+                     const void* o, const float* lse, const void* d_o,
+                     void* dq, float* dc, float* dw, float* dgamma,
+                     const void* ws_saved, size_t saved_bytes,
+                     void* ws_bwd, size_t bwd_bytes, void* stream);
+
+/* Synchronise `stream` and report a launch error or a device wait that gave
+ * up since the last check on this device (and clear the flag). */
+laga_status laga_sync_check(void* stream);
+
+/* Static text for a status code. */
+const char* laga_status_string(laga_status status);
+
+/* Number of kernel launches the last laga_fwd / laga_bwd call on this host
+ * thread enqueued (0 after an error).  For launch accounting. */
+int laga_last_launch_count(void);
+
+/* Per-kernel timing for measurement.  While enabled, every kernel the
+ * library launches is bracketed by two CUDA events recorded on its own
+ * stream; laga_profile_read() waits for those events and returns, per kernel
+ * name, the summed elapsed milliseconds and the launch count since the last
+ * laga_profile_reset().  Names are static strings.  Returns the number of
+ * distinct kernels (at most max are written).  Off by default. */
+void laga_profile_enable(int on);
+void laga_profile_reset(void);
+int laga_profile_read(const char** names, double* total_ms, int* launches, int max);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LAGA_H */

@@ -188,7 +188,7 @@ def forward(q, c, w, gamma, cos, sin, dims: Dims, heads=None, block=512):
     """
     st = _prologue(q, c, w, gamma, cos, sin, dims)
     B, S, H = dims.B, dims.S, dims.H
-    KV = np.einsum("bsk,khd->bshd", st["L"], st["W"])        # [B,S,H,dh]
+    KV = np.einsum("bsk,khd->bshd", st["L"], st["W"], optimize=True)        # [B,S,H,dh]
     k_nope = KV[..., :dims.d_nope]
     v = KV[..., dims.d_nope:]
     O = np.full((B, S, H, dims.d_v), np.nan)
@@ -260,13 +260,13 @@ def backward(saved, dO, block=512):
     dq = np.concatenate([dq_nope, rope_transpose(dq_rope_r, saved["cos"], saved["sin"])],
                         axis=-1)
     out = dict(dq=dq, dKV=dKV, delta=delta, dkpe_r_heads=dkpe_r_h)
-    dW = np.einsum("bsk,bshd->khd", saved["L"], np.nan_to_num(dKV, nan=0.0))
+    dW = np.einsum("bsk,bshd->khd", saved["L"], np.nan_to_num(dKV, nan=0.0), optimize=True)
     dW[:, [h for h in range(H) if h not in set(hs)], :] = np.nan
     out["dw"] = dW.reshape(dims.d_kv, H * dims.d_head_kv)
     if saved["heads"] is not None:
         out.update(dc=None, dgamma=None, dL=None)
         return out
-    dL = np.einsum("bshd,khd->bsk", dKV, saved["W"])
+    dL = np.einsum("bshd,khd->bsk", dKV, saved["W"], optimize=True)
     dx, dgamma = layernorm_backward(dL, saved["xhat"], saved["rstd"], saved["gamma"])
     dkpe_r = dkpe_r_h.sum(axis=2)
     dkpe = rope_transpose(dkpe_r, saved["cos"], saved["sin"])
@@ -292,7 +292,7 @@ def forward_absorbed(q, c, w, gamma, cos, sin, dims: Dims, block=512):
     B, S, H = dims.B, dims.S, dims.H
     Wk = st["W"][..., :dims.d_nope]                          # [d_kv,H,d_nope]
     Wv = st["W"][..., dims.d_nope:]                          # [d_kv,H,d_v]
-    q_abs = np.einsum("bshd,khd->bshk", st["q_nope"], Wk)    # [B,S,H,d_kv]
+    q_abs = np.einsum("bshd,khd->bshk", st["q_nope"], Wk, optimize=True)    # [B,S,H,d_kv]
     o_lat = np.zeros((B, S, H, dims.d_kv))
     LSE = np.zeros((B, H, S))
     sc = dims.sm_scale
@@ -308,7 +308,7 @@ def forward_absorbed(q, c, w, gamma, cos, sin, dims: Dims, block=512):
                 l = p.sum(axis=1)
                 LSE[b, h, r0:r1] = m + np.log(l)
                 o_lat[b, r0:r1, h] = (p / l[:, None]) @ st["L"][b, :r1]
-    O = np.einsum("bshk,khd->bshd", o_lat, Wv)
+    O = np.einsum("bshk,khd->bshd", o_lat, Wv, optimize=True)
     st.update(q_abs=q_abs, o_lat=o_lat, O=O, LSE=LSE, Wk=Wk, Wv=Wv, dims=dims)
     return O, LSE, st
 
@@ -321,8 +321,8 @@ def backward_absorbed(saved, dO, block=512):
     L, kr, qr = saved["L"], saved["kpe_r"], saved["q_rope_r"]
     q_abs, o_lat, LSE = saved["q_abs"], saved["o_lat"], saved["LSE"]
     sc = dims.sm_scale
-    dWv = np.einsum("bshk,bshd->khd", o_lat, dO)
-    do_lat = np.einsum("bshd,khd->bshk", dO, saved["Wv"])
+    dWv = np.einsum("bshk,bshd->khd", o_lat, dO, optimize=True)
+    do_lat = np.einsum("bshd,khd->bshk", dO, saved["Wv"], optimize=True)
     delta = (dO * saved["O"]).sum(axis=-1)
     dq_abs = np.zeros_like(q_abs)
     dq_rope_r = np.zeros_like(qr)
@@ -341,8 +341,8 @@ def backward_absorbed(saved, dO, block=512):
                 dq_rope_r[b, r0:r1, h] = sc * (dS @ kr[b, :r1])
                 dLat[b, :r1] += sc * (dS.T @ q_abs[b, r0:r1, h]) + P.T @ do_lat[b, r0:r1, h]
                 dkpe_r[b, :r1] += sc * (dS.T @ qr[b, r0:r1, h])
-    dWk = np.einsum("bshk,bshd->khd", dq_abs, saved["q_nope"])
-    dq_nope = np.einsum("bshk,khd->bshd", dq_abs, saved["Wk"])
+    dWk = np.einsum("bshk,bshd->khd", dq_abs, saved["q_nope"], optimize=True)
+    dq_nope = np.einsum("bshk,khd->bshd", dq_abs, saved["Wk"], optimize=True)
     dq = np.concatenate([dq_nope, rope_transpose(dq_rope_r, saved["cos"], saved["sin"])],
                         axis=-1)
     dW = np.concatenate([dWk, dWv], axis=-1).reshape(dims.d_kv, H * dims.d_head_kv)
