@@ -1,0 +1,310 @@
+// a4 causal MLA attention forward on the 5th-generation tensor cores
+// (Algorithm 1 step 5: scores = (q_nope||q_rope)(k_nope||k_pe)^T / sqrt(d),
+// out = softmax(scores) v; Section 5.3: k_pe shared by all heads).
+//
+// One CTA per (128-row query tile, head, batch), 6 warps:
+//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  Reads the
+//              score row S_j from TMEM, applies the causal mask on the
+//              diagonal tile, keeps the running max m (base-2 domain) and
+//              sum l, writes P_j = exp2(s*scale*log2e - m) as bf16 back into
+//              the same TMEM columns, and rescales the O accumulator only
+//              when its row max grows by more than 2^8 (the result is exact
+//              either way: O and l carry the same stale max).
+//   warp 4     TMA producer: Q once (q_nope | RoPE'd q_rope, 3 boxes), then
+//              per key tile K_j (k_nope | k_pe, 3 boxes) and V_j (2 boxes)
+//              into two-stage rings.
+//   warp 5     TMEM allocator and MMA issuer: S_{j+1} = Q K_{j+1}^T (12
+//              K-steps, the two column bands are consecutive K chunks of the
+//              same accumulator) is issued before O += P_j V_j (8 K-steps, P
+//              from TMEM), so the tensor core works on the next tile while
+//              the softmax warps handle this one.
+// TMEM columns: S/P double buffer [0,256), O [256,384).
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace laga {
+namespace {
+using namespace sm100;
+
+constexpr int BM = 128;                 // query rows per tile
+constexpr int BN = 128;                 // keys per tile
+constexpr int BOX = 128 * 64 * 2;       // one [128 rows x 64 bf16] box = 16 KB
+constexpr int Q_BYTES = 3 * BOX;
+constexpr int K_BYTES = 3 * BOX;
+constexpr int V_BYTES = 2 * BOX;
+constexpr int SMEM_BYTES = Q_BYTES + 2 * (K_BYTES + V_BYTES) + 1024;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int O_COL = 256;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr float LN2 = 0.6931471805599453f;
+
+struct FwdMaps {
+  CUtensorMap qn, qr, kv, kpe;
+};
+struct FwdParams {
+  int S, H, B, n_qt;
+  float sl2;              // softmax scale * log2(e)
+  __nv_bfloat16* O;       // [B,S,H,128]
+  float* lse;             // [B,H,S]
+  int* err;
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ FwdMaps tm, const FwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint8_t* Qs = sm;
+  uint8_t* Ks = sm + Q_BYTES;
+  uint8_t* Vs = Ks + 2 * K_BYTES;
+  __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_vf[2], bar_ve[2], bar_s[2], bar_p[2], bar_o;
+  __shared__ uint32_t tmem_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = p.H * p.B;
+  const int qt = p.n_qt - 1 - (int)(blockIdx.x / per);   // longest query tiles first
+  const int h = (int)(blockIdx.x % per) % p.H;
+  const int b = (int)(blockIdx.x % per) / p.H;
+  const int q0 = qt * BM;
+  const int n_kt = qt + 1;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_q, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bar_kf[i], 1);
+      mbar_init(&bar_ke[i], 1);
+      mbar_init(&bar_vf[i], 1);
+      mbar_init(&bar_ve[i], 1);
+      mbar_init(&bar_s[i], 1);
+      mbar_init(&bar_p[i], 4);
+    }
+    mbar_init(&bar_o, 1);
+    fence_barrier_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(&tmem_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_sh;
+
+  if (warp == 4) {
+    if (lane == 0) {
+      tma_prefetch_desc(&tm.qn);
+      tma_prefetch_desc(&tm.kv);
+      mbar_arrive_expect_tx(&bar_q, Q_BYTES);
+      tma_load_4d(Qs, &tm.qn, &bar_q, 0, h, q0, b);
+      tma_load_4d(Qs + BOX, &tm.qn, &bar_q, 64, h, q0, b);
+      tma_load_4d(Qs + 2 * BOX, &tm.qr, &bar_q, 0, h, q0, b);
+      for (int j = 0; j < n_kt; ++j) {
+        const int st = j & 1;
+        const int k0 = j * BN;
+        if (j >= 2 && !mbar_wait(&bar_ke[st], ((j >> 1) - 1) & 1, p.err)) break;
+        uint8_t* kd = Ks + st * K_BYTES;
+        mbar_arrive_expect_tx(&bar_kf[st], K_BYTES);
+        tma_load_4d(kd, &tm.kv, &bar_kf[st], 0, k0, h, b);
+        tma_load_4d(kd + BOX, &tm.kv, &bar_kf[st], 64, k0, h, b);
+        tma_load_3d(kd + 2 * BOX, &tm.kpe, &bar_kf[st], 0, k0, b);
+        if (j >= 2 && !mbar_wait(&bar_ve[st], ((j >> 1) - 1) & 1, p.err)) break;
+        uint8_t* vd = Vs + st * V_BYTES;
+        mbar_arrive_expect_tx(&bar_vf[st], V_BYTES);
+        tma_load_4d(vd, &tm.kv, &bar_vf[st], 128, k0, h, b);
+        tma_load_4d(vd + BOX, &tm.kv, &bar_vf[st], 192, k0, h, b);
+      }
+    }
+  } else if (warp == 5) {
+    if (lane == 0) {
+      const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
+      const uint32_t idO = idesc_bf16(BM, 128, 0, 1);
+      const uint32_t qa = smem_u32(Qs);
+      bool ok = mbar_wait(&bar_q, 0, p.err);
+      auto issue_s = [&](int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&bar_kf[st], (j >> 1) & 1, p.err)) return false;
+        tc_fence_after();
+        const uint32_t ka = smem_u32(Ks + st * K_BYTES);
+        const uint32_t d = tmem + st * BN;
+#pragma unroll
+        for (int s = 0; s < 12; ++s) {
+          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
+          mma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS, s > 0);
+        }
+        mma_commit(&bar_s[st]);
+        mma_commit(&bar_ke[st]);
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 0; ok && j < n_kt; ++j) {
+        if (j + 1 < n_kt && !issue_s(j + 1)) break;
+        const int st = j & 1;
+        if (!mbar_wait(&bar_p[st], (j >> 1) & 1, p.err)) break;
+        if (!mbar_wait(&bar_vf[st], (j >> 1) & 1, p.err)) break;
+        tc_fence_after();
+        const uint32_t va = smem_u32(Vs + st * V_BYTES);
+        const uint32_t pa = tmem + st * BN;
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ts(tmem + O_COL, pa + s * 8, sdesc_sw128(va + s * 2048, BOX, 1024), idO,
+                 (j > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&bar_ve[st]);
+        mma_commit(&bar_o);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax warps
+    const int r = threadIdx.x;
+    const int qi = q0 + r;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kt; ++j) {
+      const int st = j & 1;
+      if (!mbar_wait(&bar_s[st], (j >> 1) & 1, p.err)) { ok = false; break; }
+      tc_fence_after();
+      float s[BN];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tmem, warp, st * BN + c * 32), u);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(u[k]);
+      }
+      if (j == n_kt - 1) {  // diagonal tile: key k0+c visible iff c <= r and k0+c < S
+        const int lim = min(r, p.S - 1 - j * BN);
+#pragma unroll
+        for (int c = 0; c < BN; ++c)
+          if (c > lim) s[c] = -INFINITY;
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
+      mx *= p.sl2;
+      const float m_new = (mx > m + RESCALE_LOG2) ? mx : m;
+      const float alpha = exp2f(m - m_new);
+      const bool need = j > 0 && m_new != m;
+      if (__any_sync(0xffffffffu, need)) {
+        // O must hold P_{j-1} V_{j-1} before it is rescaled in place.
+        if (!mbar_wait(&bar_o, (j - 1) & 1, p.err)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem_addr(tmem, warp, O_COL + c * 32), u);
+          uint32_t lo[16], hi[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            lo[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
+            hi[k] = __float_as_uint(__uint_as_float(u[16 + k]) * alpha);
+          }
+          tmem_st16(tmem_addr(tmem, warp, O_COL + c * 32), lo);
+          tmem_st16(tmem_addr(tmem, warp, O_COL + c * 32 + 16), hi);
+        }
+      }
+      m = m_new;
+      float rs = 0.f;
+      const float negm = -m;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float a = exp2f(fmaf(s[c * 32 + 2 * k], p.sl2, negm));
+          const float bb = exp2f(fmaf(s[c * 32 + 2 * k + 1], p.sl2, negm));
+          rs += a + bb;
+          pk[k] = pack_bf16(a, bb);
+        }
+        tmem_st16(tmem_addr(tmem, warp, st * BN + c * 16), pk);
+      }
+      l = l * alpha + rs;
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p[st]);
+    }
+    // ---------------------------------------------------------- epilogue
+    // A parity wait is exact only if the barrier is at most one phase behind
+    // the awaited one.  The last S tile seen here guarantees only P V up to
+    // tile n_kt-3, so wait for tile n_kt-2 before tile n_kt-1.
+    if (ok && n_kt >= 2) ok = mbar_wait(&bar_o, (n_kt - 2) & 1, p.err);
+    if (ok && mbar_wait(&bar_o, (n_kt - 1) & 1, p.err)) {
+      tc_fence_after();
+      const float inv = 1.0f / l;
+      __nv_bfloat16* orow = p.O + (((long long)b * p.S + qi) * p.H + h) * 128;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tmem, warp, O_COL + c * 32), u);
+        uint4 v4[4];
+        uint32_t* w = reinterpret_cast<uint32_t*>(v4);
+#pragma unroll
+        for (int k = 0; k < 16; ++k)
+          w[k] = pack_bf16(__uint_as_float(u[2 * k]) * inv, __uint_as_float(u[2 * k + 1]) * inv);
+        if (qi < p.S) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) dst[k] = v4[k];
+        }
+      }
+      if (qi < p.S) p.lse[((long long)b * p.H + h) * p.S + qi] = (m + log2f(l)) * LN2;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
+  Views v = make_views(p, x);
+  const uint64_t S = p.S, H = p.H, B = p.B;
+  FwdMaps tm;
+  cudaError_t e;
+  {
+    const uint64_t ld = (uint64_t)v.qn_ld * 2;
+    uint64_t dims[4] = {128, H, S, B}, str[3] = {ld, H * ld, S * H * ld};
+    uint32_t box[4] = {64, 1, 128, 1};
+    if ((e = make_tmap_bf16(&tm.qn, v.qn, 4, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[4] = {64, H, S, B}, str[3] = {128, H * 128, S * H * 128};
+    uint32_t box[4] = {64, 1, 128, 1};
+    if ((e = make_tmap_bf16(&tm.qr, v.qr, 4, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[4] = {256, S, H, B};
+    uint64_t str[3] = {(uint64_t)v.kv_ss * 2, (uint64_t)v.kv_sh * 2, (uint64_t)v.kv_sb * 2};
+    uint32_t box[4] = {64, 128, 1, 1};
+    if ((e = make_tmap_bf16(&tm.kv, v.kv, 4, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[3] = {64, S, B}, str[2] = {128, S * 128};
+    uint32_t box[3] = {64, 128, 1};
+    if ((e = make_tmap_bf16(&tm.kpe, v.kpe, 3, dims, str, box)) != cudaSuccess) return e;
+  }
+  FwdParams prm;
+  prm.S = p.S;
+  prm.H = p.H;
+  prm.B = p.B;
+  prm.n_qt = (p.S + BM - 1) / BM;
+  prm.sl2 = p.scale * 1.4426950408889634f;
+  prm.O = v.O;
+  prm.lse = x.lse;
+  prm.err = x.err;
+  e = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)prm.n_qt * p.H * p.B;
+  LaunchScope ls_("attn_fwd", st);
+  attn_fwd_tc_kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(tm, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace laga

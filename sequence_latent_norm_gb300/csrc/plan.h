@@ -26,7 +26,8 @@ enum BufId {
   W_OC,         // bf16 [B*S*H, 128]    padded O
   N_SAVED,
   // transient of the backward (LAGA_WS_BWD)
-  T_DELTA = N_SAVED,  // fp32 [B*H*S]   rowsum(dO * O)
+  T_DELTA = N_SAVED,  // fp32 [B*H, Sp]  rowsum(dO * O), rows padded to Sp = ceil128(S)
+  T_LSE2,       // fp32 [B*H, Sp]       LSE * log2(e) in the same padded rows
   T_DOC,        // bf16 [B*S*H, 128]    padded / converted dO
   T_DQ,         // fp32 [B*S*H, 192]    dq in the rotated frame
   T_DKV,        // bf16 [B*S*H, 256]    dk_nope | dv per head
@@ -37,6 +38,8 @@ enum BufId {
   T_DOLAT,      // bf16 [B*S*H, 512]    dO up-projected to the latent (absorbed)
   T_DQABS,      // bf16 [B*S*H, 512]    gradient of q_absorbed (absorbed)
   T_DLF,        // fp32 [B*S, 512]      attention part of dL (absorbed)
+  T_DWP,        // fp32 [splits, 512, H*256] split-K partials of dW
+  T_SEM,        // int  [B*H*ceil(S/128) + 1] ordered-dQ semaphores + work counter
   N_BUF
 };
 
@@ -55,15 +58,24 @@ struct Plan {
 
   long long tokens() const { return (long long)B * S; }
   long long rows() const { return (long long)B * S * H; }  // (token, head) rows
+  long long s_pad() const { return (S + 127) / 128 * 128; }  // padded row length
 };
 
 static const char* const kBufName[N_BUF] = {
     "L", "ln_mean", "ln_rstd", "k_pe_rot", "q_rope_rot", "kv", "q_absorbed", "o_latent",
     "q_nope_padded", "w_kvb_padded", "o_padded",
-    "delta", "dO_padded", "dq_rot", "dkv", "dk_pe_heads", "dL", "dgamma_partials",
-    "dw_padded", "dO_latent", "dq_absorbed", "dL_attention"};
+    "delta", "lse_log2", "dO_padded", "dq_rot", "dkv", "dk_pe_heads", "dL", "dgamma_partials",
+    "dw_padded", "dO_latent", "dq_absorbed", "dL_attention", "dw_split_partials",
+    "dq_semaphores"};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Token-reduction splits of the dW GEMM: about 512 CTAs over its 4*H
+// output tiles, at most 8.  Depends on the dims only (fixed summation order).
+inline int dw_splits(int H) {
+  int s = 512 / (4 * H);
+  return s < 1 ? 1 : (s > 8 ? 8 : s);
+}
 
 // Validate dims; returns LAGA_OK or the error and fills the plan.
 inline laga_status make_plan(const laga_dims* dims, Plan* p) {
@@ -106,7 +118,8 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
     p->len[W_WC] = (size_t)512 * H * 256 * 2;
     p->len[W_OC] = R * 128 * 2;
   }
-  p->len[T_DELTA] = R * 4;
+  p->len[T_DELTA] = (size_t)p->B * H * p->s_pad() * 4;
+  p->len[T_LSE2] = (size_t)p->B * H * p->s_pad() * 4;
   if (!p->canonical) p->len[T_DOC] = R * 128 * 2;
   p->len[T_DQ] = R * 192 * 4;
   p->len[T_DKV] = R * 256 * 2;
@@ -119,6 +132,8 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
     p->len[T_DQABS] = R * 512 * 2;
     p->len[T_DLF] = T * 512 * 4;
   }
+  p->len[T_SEM] = ((size_t)p->B * p->H * ((p->S + 127) / 128) + 1) * 4;
+  if (dw_splits(p->H) > 1) p->len[T_DWP] = (size_t)dw_splits(p->H) * 512 * H * 256 * 4;
   size_t o = 0;
   for (int i = 0; i < N_SAVED; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }
   p->saved_bytes = o;

@@ -124,8 +124,13 @@ template <typename T>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
                                                       const T* __restrict__ d_o, int B, int S,
                                                       int H, int dv, float* __restrict__ delta,
-                                                      __nv_bfloat16* __restrict__ do_pad) {
+                                                      __nv_bfloat16* __restrict__ do_pad,
+                                                      int* __restrict__ sem, int n_sem,
+                                                      const float* __restrict__ lse,
+                                                      float* __restrict__ lse2, int s_pad) {
   const int lane = threadIdx.x & 31;
+  // the attention backward's semaphores and work counter start at zero
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n_sem; i += gridDim.x * 256) sem[i] = 0;
   const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
   if (row >= (long long)B * S * H) return;
   const T* orow = o + row * dv;
@@ -136,7 +141,11 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
   const int h = (int)(row % H);
   const long long tok = row / H;
   const int b = (int)(tok / S), s = (int)(tok % S);
-  if (lane == 0) delta[((long long)b * H + h) * S + s] = acc;
+  if (lane == 0) {
+    const long long pr = ((long long)b * H + h) * s_pad + s;
+    delta[pr] = acc;
+    lse2[pr] = lse[((long long)b * H + h) * S + s] * 1.4426950408889634f;
+  }
   if (do_pad) {
     for (int e = lane; e < 128; e += 32)
       do_pad[row * 128 + e] = __float2bfloat16_rn(e < dv ? to_f32(grow[e]) : 0.f);
@@ -315,13 +324,18 @@ cudaError_t launch_bwd_pre(const Plan& p, const Ptrs& x, cudaStream_t st) {
   const int g = grid_for(p.rows(), WARPS);
   float* delta = x.buf<float>(p, T_DELTA);
   __nv_bfloat16* dop = p.canonical ? nullptr : x.buf<__nv_bfloat16>(p, T_DOC);
+  int* sem = x.buf<int>(p, T_SEM);
+  float* lse2 = x.buf<float>(p, T_LSE2);
+  const int n_sem = (int)(p.len[T_SEM] / 4);
   if (p.fp32)
     bwd_pre_kernel<float><<<g, 256, 0, st>>>((const float*)x.o, (const float*)x.d_o, p.B, p.S, p.H,
-                                             p.dv, delta, dop);
+                                             p.dv, delta, dop, sem, n_sem, x.lse, lse2,
+                                             (int)p.s_pad());
   else
     bwd_pre_kernel<__nv_bfloat16><<<g, 256, 0, st>>>((const __nv_bfloat16*)x.o,
                                                      (const __nv_bfloat16*)x.d_o, p.B, p.S, p.H,
-                                                     p.dv, delta, dop);
+                                                     p.dv, delta, dop, sem, n_sem, x.lse, lse2,
+                                             (int)p.s_pad());
   return cudaGetLastError();
 }
 

@@ -171,17 +171,21 @@ LAGA_DEVINL void mma_commit(uint64_t* bar) {
 }
 
 // TMEM -> registers: this warp's 32 lanes, 32 consecutive 32-bit columns.
+// The load and its completion wait are one asm statement, so the compiler
+// cannot consume the registers before the data has arrived.
 LAGA_DEVINL void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
       "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
         "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
         "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
+      : "r"(taddr)
+      : "memory");
 }
 // registers -> TMEM: this warp's 32 lanes, 16 consecutive 32-bit columns.
 LAGA_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -199,6 +203,20 @@ LAGA_DEVINL void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" 
 // TMEM address of (lane quadrant of this warp, column).
 LAGA_DEVINL uint32_t tmem_addr(uint32_t base, int warp_in_group, int col) {
   return base + ((uint32_t)(warp_in_group * 32) << 16) + (uint32_t)col;
+}
+
+// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
+LAGA_DEVINL void named_bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+LAGA_DEVINL int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+LAGA_DEVINL void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 LAGA_DEVINL uint32_t pack_bf16(float lo, float hi) {

@@ -74,21 +74,53 @@ def oracle_run(wl: Workload, cpu=None, heads=None):
     O, LSE, st = oracle.forward(a["q"], a["c"], a["w"], a["gamma"], a["cos"], a["sin"], d,
                                 heads=heads)
     g = oracle.backward(st, a["dO"])
-    return dict(O=O, LSE=LSE, dq=g["dq"], dc=g["dc"], dw=g["dw"], dgamma=g["dgamma"])
+    vmax = running_vmax(st["KV"][..., wl.d_nope:])
+    return dict(O=O, LSE=LSE, dq=g["dq"], dc=g["dc"], dw=g["dw"], dgamma=g["dgamma"], vmax=vmax)
+
+
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    ax = np.maximum(np.abs(np.asarray(x, np.float64)), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def o_abs_bound(Or, vmax):
+    """Per-element max-abs bound on O: 1e-2, except where bf16 storage alone
+    cannot resolve 1e-2.  O_i is a convex combination of the v_j (j <= i),
+    which are stored in bf16 (half an ulp of |v_j|) and computed from the
+    bf16-rounded normalised latent (about another half ulp); O is rounded
+    to bf16 on output (half an ulp of |O|).  ``vmax`` is max_{j<=i} |v_jd|
+    from the oracle, so the bound is max(1e-2, ulp(vmax) + ulp(|O|)/2)."""
+    return np.maximum(O_MAX_ABS, bf16_ulp(vmax) + 0.5 * bf16_ulp(Or))
+
+
+def running_vmax(v):
+    """max over keys j <= i of |v[b, j, h, d]| (v: [B, S, H, d_v])."""
+    return np.maximum.accumulate(np.abs(v), axis=1)
 
 
 def check_forward(got, ref, where=""):
     O, Or = as_f64(got["O"]), ref["O"]
-    assert max_abs(O, Or) <= O_MAX_ABS, f"{where} O max-abs {max_abs(O, Or):.3e}"
+    excess = np.abs(O - Or) - o_abs_bound(Or, ref["vmax"])
+    assert excess.max() <= 0, (f"{where} O max-abs {max_abs(O, Or):.3e} exceeds its bound by "
+                               f"{excess.max():.3e}")
     assert rel_fro(O, Or) <= O_REL_FRO, f"{where} O rel-fro {rel_fro(O, Or):.3e}"
     L, Lr = as_f64(got["LSE"]), ref["LSE"]
     assert max_abs(L, Lr) <= LSE_MAX_ABS, f"{where} LSE max-abs {max_abs(L, Lr):.3e}"
 
 
+GRAD_ABS_RMS = 1e-4
+
+
 def check_grads(got, ref, keys=("dq", "dc", "dw", "dgamma"), where=""):
+    """Relative Frobenius error <= 1e-2, with an absolute floor of 1e-4 RMS
+    per element for references that vanish (one token: dS = dO.v - dO.O = 0
+    exactly, so dq is identically zero)."""
     for k in keys:
-        e = rel_fro(as_f64(got[k]), ref[k])
-        assert e <= GRAD_REL_FRO, f"{where} {k} rel-fro {e:.3e}"
+        g, r = as_f64(got[k]), ref[k]
+        err = float(np.linalg.norm(g - r))
+        lim = GRAD_REL_FRO * float(np.linalg.norm(r)) + GRAD_ABS_RMS * np.sqrt(r.size)
+        assert err <= lim, f"{where} {k} rel-fro {rel_fro(g, r):.3e} (abs {err:.3e} > {lim:.3e})"
 
 
 def head_slice(x, h, axis):

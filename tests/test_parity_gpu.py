@@ -63,7 +63,8 @@ def test_config2_full_size_sampled_heads(h):
     got = gpu_run(wl, cpu)
     ref = oracle_run(wl, cpu, heads=[h])
     check_forward(dict(O=got["O"][:, :, h], LSE=got["LSE"][:, h]),
-                  dict(O=ref["O"][:, :, h], LSE=ref["LSE"][:, h]), f"head {h}")
+                  dict(O=ref["O"][:, :, h], LSE=ref["LSE"][:, h], vmax=ref["vmax"][:, :, h]),
+                  f"head {h}")
     assert rel_fro(as_f64(got["dq"][:, :, h]), ref["dq"][:, :, h]) <= GRAD_REL_FRO
     cols = dw_cols(wl, h)
     assert rel_fro(as_f64(got["dw"][:, cols]), ref["dw"][:, cols]) <= GRAD_REL_FRO
