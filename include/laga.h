@@ -151,6 +151,36 @@ const char* laga_status_string(laga_status status);
  * thread enqueued (0 after an error).  For launch accounting. */
 int laga_last_launch_count(void);
 
+/* LayerNorm + RoPE backward (the backward of steps a1-a2 alone) for callers
+ * that cannot allocate device memory, e.g. a runtime that has reserved the
+ * whole device for its own pool and forbids cudaMalloc during a step, or an
+ * embedding that owns only the tensors it passes in.  The paper has no
+ * counterpart of this entry point; it exists for such callers.
+ *
+ * Instead of a caller workspace it uses a fixed scratch array inside the
+ * library (296 x 512 fp32 = 592 KiB per device, held from the first call on
+ * that device until the process exits) and calls no cudaMalloc, cudaFree or
+ * allocating library routine.  The first call on a device looks up the
+ * scratch's device address (once, with that device current); make that
+ * first call before any stream capture.  All calls share the scratch: calls
+ * whose kernels may overlap on the GPU race on it and must be ordered by the
+ * caller.  Each call rewrites all the scratch it reads, so no state carries
+ * over between calls.
+ *   c           [B, S, d_kv + d_rope]       io dtype, as given to laga_fwd
+ *   gamma       [d_kv] fp32; cos, sin [S, d_rope/2] fp32
+ *   d_latent    [B, S, d_kv] fp32: gradient with respect to the normalised
+ *               latent L = LayerNorm(latent) * gamma
+ *   d_kpe_rot   [B, S, n_h_shard, d_rope] fp32: each head's gradient with
+ *               respect to the RoPE'd k_pe (summed over heads in head order)
+ *   dc          [B, S, d_kv + d_rope] fp32 (output), dgamma [d_kv] fp32 (output)
+ * The LayerNorm statistics are recomputed from c.  d_kv above 512 does not
+ * fit the scratch and returns LAGA_ERR_WORKSPACE; other errors as for
+ * laga_bwd. */
+laga_status laga_norm_rope_bwd_noalloc(const laga_dims* dims, const void* c, const float* gamma,
+                                       const float* cos, const float* sin,
+                                       const float* d_latent, const float* d_kpe_rot,
+                                       float* dc, float* dgamma, void* stream);
+
 /* Per-kernel timing for measurement.  While enabled, every kernel the
  * library launches is bracketed by two CUDA events recorded on its own
  * stream; laga_profile_read() waits for those events and returns, per kernel

@@ -22,7 +22,8 @@ WS_SAVED, WS_BWD = 0, 1
 
 EXPORTED = ("laga_workspace_bytes", "laga_workspace_tensor", "laga_fwd", "laga_bwd",
             "laga_sync_check", "laga_status_string", "laga_last_launch_count",
-            "laga_profile_enable", "laga_profile_reset", "laga_profile_read")
+            "laga_profile_enable", "laga_profile_reset", "laga_profile_read",
+            "laga_norm_rope_bwd_noalloc")
 
 
 class LagaDims(ctypes.Structure):
@@ -75,6 +76,8 @@ def load(path: str = LIB_PATH):
     lib.laga_profile_read.argtypes = [ctypes.POINTER(ctypes.c_char_p),
                                       ctypes.POINTER(ctypes.c_double), ctypes.POINTER(I), I]
     lib.laga_profile_read.restype = I
+    lib.laga_norm_rope_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P]
+    lib.laga_norm_rope_bwd_noalloc.restype = I
     _lib = lib
     return lib
 
@@ -150,3 +153,12 @@ def profile_read():
     cnt = (ctypes.c_int * n)()
     k = lib.laga_profile_read(names, ms, cnt, n)
     return {names[i].decode(): (ms[i], cnt[i]) for i in range(min(k, n))}
+
+
+def norm_rope_bwd_noalloc(dims: LagaDims, c, gamma, cos, sin, d_latent, d_kpe_rot, dc, dgamma,
+                          stream=0):
+    """laga_norm_rope_bwd_noalloc with raw device addresses (ints): the
+    LayerNorm + RoPE backward using the library's own fixed scratch."""
+    _check(load().laga_norm_rope_bwd_noalloc(ctypes.byref(dims), c, gamma, cos, sin, d_latent,
+                                             d_kpe_rot, dc, dgamma, stream),
+           "laga_norm_rope_bwd_noalloc")
