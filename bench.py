@@ -214,6 +214,25 @@ def run_reference(args, rank):
     print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- ranks
+def rank_workload(base, rank: int, world: int):
+    """Rank r computes heads [r*H, (r+1)*H) of a world*H-head layer: the
+    shards partition the heads, no data-path collective (weak scaling)."""
+    import dataclasses
+    return dataclasses.replace(base, n_h_total=base.H * world, head_offset=base.H * rank)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The slowest rank's time (the job's time) on every rank."""
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import dataclasses
@@ -225,8 +244,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     base = config(args.config)
-    # each rank computes its own head shard of a world*H-head layer
-    wl = dataclasses.replace(base, n_h_total=base.H * world, head_offset=base.H * rank)
+    wl = rank_workload(base, rank, world)
     S, H, B = wl.S, wl.H, wl.B
 
     # CPU baseline first (rank 0, one GPU only): the oracle as it stands.
@@ -300,11 +318,7 @@ def run_ours(args, rank, world, local_rank):
     prof = pkg._lib.profile_read()
     pkg._lib.sync_check()
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    total_ms = sum(step_ms)
-    if world > 1:
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
     fwd_f, bwd_f = attention_flops(S, H, B)
     attn_flops = fwd_f + bwd_f

@@ -4,23 +4,25 @@
 //   dQ = dS K,    dK = dS^T Q   (the k_pe band of dK kept per head).
 //
 // One CTA per (128-key tile j, head h, batch b), taken from a global work
-// counter in order of increasing j (longest first).  It walks the query
+// counter in order of increasing j (longest first); it walks the query
 // tiles i = j .. last.  10 warps:
-//   warps 0-3  "softmax": thread r owns key row r.  Reads S^T = K Q_i^T and
-//              dP^T = V dO_i^T rows from TMEM, forms P^T (bf16, written back
-//              into the S^T columns for the TMEM-operand MMA) and
-//              dS^T * scale (bf16, written to shared memory, 128-byte
-//              swizzled, for the shared-memory-operand MMAs).
-//   warps 4-7  "dQ": read dQ_i = dS K_j (query rows) and the k_pe part of
-//              dK_j for this i (key rows) from TMEM; add dQ_i into the fp32
-//              dQ accumulator in global memory in a fixed order (key tile
-//              0, 1, 2, ... through a per-(b,h,i) semaphore), so every run
-//              sums identically; keep the k_pe part of dK in registers.
-//   warp 8     TMA producer: K_j, V_j once; Q_i, dO_i, LSE_i, delta_i per i.
+//   warps 0-7  compute.  Warp w owns TMEM lane quadrant w%4 (key rows for
+//              S^T, dP^T, dK; query rows for dQ) and column half w/4.
+//              Phase A: S^T -> P^T (bf16 into TMEM for the TMEM-operand
+//              MMA of dV).  Phase B: dP^T -> dS^T * scale (bf16 into shared
+//              memory, 128-byte swizzled).  Phase C: copy dQ_i and this
+//              tile's k_pe part of dK out of TMEM into registers and free
+//              the columns, then add dQ_i into the fp32 dQ accumulator in
+//              global memory in a fixed order: key tile 0, 1, 2, ... through
+//              a per-(b,h,i) semaphore, so every run sums identically.  The
+//              adds are TMA tensor reduce-adds (a store for key tile 0) from
+//              a swizzled fp32 staging tile, three 64-column chunks per i.
+//   warp 8     TMA producer: K_j, V_j once; per i: Q_i, dO_i, LSE_i, delta_i.
 //   warp 9     TMEM allocator and MMA issuer.
-// TMEM columns: dV [0,128), dK_nope [128,256), S^T -> P^T [256,384),
-// dP^T [384,512); after the softmax warps are done: dK_rope_i [256,320),
-// dQ_i [320,512).
+// TMEM columns: dV [0,128), dK_nope [128,256), S^T [256,384) with P^T in
+// [256,288) and [320,352), dP^T [384,512); after the softmax phases the
+// k_pe part of dK for this i goes to [256,320) and dQ_i to [320,512).
+// Every mbarrier is waited phase by phase, so parity waits are exact.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -35,20 +37,23 @@ constexpr int BOX = 128 * 64 * 2;        // 16 KB
 constexpr int K_OFF = 0;                 // K_j: 3 boxes
 constexpr int V_OFF = 3 * BOX;           // V_j: 2 boxes
 constexpr int Q_OFF = 5 * BOX;           // Q_i: 3 boxes
-constexpr int DO_OFF = 8 * BOX;          // dO_i: 2 boxes
-constexpr int DS_OFF = 10 * BOX;         // dS^T: 2 boxes
-constexpr int LSE_OFF = 12 * BOX;        // 128 fp32
-constexpr int DLT_OFF = LSE_OFF + 512;   // 128 fp32
-constexpr int SMEM_BYTES = DLT_OFF + 512 + 1024;
+constexpr int DS_OFF = 8 * BOX;          // dS^T: 2 boxes
+constexpr int DO_OFF = 10 * BOX;         // dO_i: 2 boxes
+constexpr int ST_OFF = 12 * BOX;         // dQ staging: 2 boxes of [128 rows x 32 fp32]
+constexpr int LD_OFF = 14 * BOX;         // LSE 512 B + delta 512 B
+constexpr int BAR_OFF = LD_OFF + 1024;   // mbarriers, TMEM address, work item
+constexpr int SMEM_BYTES = BAR_OFF + 256;  // 230656 B: within the 227 KiB per block
 constexpr int THREADS = 320;
+constexpr int N_COMPUTE = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int C_DV = 0, C_DK = 128, C_S = 256, C_DP = 384, C_DKR = 256, C_DQ = 320;
 constexpr uint32_t KV_BYTES = 5 * BOX;
-constexpr uint32_t QDO_BYTES = 5 * BOX + 1024;
-constexpr uint32_t kSpinPolls = 1u << 24;
+constexpr uint32_t Q_BYTES = 3 * BOX;
+constexpr uint32_t DO_BYTES = 2 * BOX + 1024;   // dO_i + LSE_i + delta_i
+constexpr uint32_t kSemPolls = 1u << 26;
 
 struct BwdMaps {
-  CUtensorMap qn, qr, kv, kpe, dO, lse, dlt;
+  CUtensorMap qn, qr, kv, kpe, dO, lse, dlt, dq;
 };
 struct BwdParams {
   int S, H, B, n_t;
@@ -69,25 +74,51 @@ LAGA_DEVINL uint32_t sw_chunk_off(int r, int c) {
   return (uint32_t)((c >> 3) * BOX + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// TMEM column of the P^T K-step s (16 query columns): the first 64 query
+// columns are packed at [256,288), the last 64 at [320,352).
+LAGA_DEVINL uint32_t pt_col(int s) { return s < 4 ? C_S + 8 * s : C_S + 64 + 8 * (s - 4); }
+
 __global__ void __launch_bounds__(THREADS, 1)
     attn_bwd_tc_kernel(const __grid_constant__ BwdMaps tm, const BwdParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar_kv, bar_qdo, bar_qdo_free, bar_s, bar_p, bar_dq, bar_tfree, bar_fin;
-  __shared__ uint32_t tmem_sh;
-  __shared__ int item_sh;
+  // The whole budget is used, so there is no room to align the dynamic
+  // region by hand: it must start on a 1024-byte boundary (it does when the
+  // kernel has no static shared memory).  Otherwise record the error and
+  // leave before touching shared memory.
+  extern __shared__ __align__(1024) uint8_t sm[];
+  if (smem_u32(sm) & 1023u) {
+    if (threadIdx.x == 0) atomicExch(p.err, 4);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + BAR_OFF);
+  uint64_t& bar_kv = bars[0];
+  uint64_t& bar_q_full = bars[1];
+  uint64_t& bar_q_free = bars[2];
+  uint64_t& bar_do_full = bars[3];
+  uint64_t& bar_do_free = bars[4];
+  uint64_t& bar_s = bars[7];
+  uint64_t& bar_dp = bars[8];
+  uint64_t& bar_p = bars[9];
+  uint64_t& bar_ds = bars[10];
+  uint64_t& bar_dq = bars[11];
+  uint64_t& bar_tfree = bars[12];
+  uint64_t& bar_fin = bars[13];
+  uint32_t& tmem_sh = *reinterpret_cast<uint32_t*>(sm + BAR_OFF + 128);
+  int& item_sh = *reinterpret_cast<int*>(sm + BAR_OFF + 132);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
     item_sh = atomicAdd(p.counter, 1);
     mbar_init(&bar_kv, 1);
-    mbar_init(&bar_qdo, 1);
-    mbar_init(&bar_qdo_free, 1);
+    mbar_init(&bar_q_full, 1);
+    mbar_init(&bar_q_free, 1);
+    mbar_init(&bar_do_full, 1);
+    mbar_init(&bar_do_free, 1);
     mbar_init(&bar_s, 1);
-    mbar_init(&bar_p, 4);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_p, N_COMPUTE);
+    mbar_init(&bar_ds, N_COMPUTE);
     mbar_init(&bar_dq, 1);
-    mbar_init(&bar_tfree, 4);
+    mbar_init(&bar_tfree, N_COMPUTE);
     mbar_init(&bar_fin, 1);
     fence_barrier_init();
   }
@@ -118,58 +149,65 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_load_4d(sm + V_OFF + BOX, &tm.kv, &bar_kv, 192, k0, h, b);
       for (int t = 0; t < n_i; ++t) {
         const int q0 = (j + t) * BT;
-        if (t > 0 && !mbar_wait(&bar_qdo_free, (t - 1) & 1, p.err)) break;
-        mbar_arrive_expect_tx(&bar_qdo, QDO_BYTES);
-        tma_load_4d(sm + Q_OFF, &tm.qn, &bar_qdo, 0, h, q0, b);
-        tma_load_4d(sm + Q_OFF + BOX, &tm.qn, &bar_qdo, 64, h, q0, b);
-        tma_load_4d(sm + Q_OFF + 2 * BOX, &tm.qr, &bar_qdo, 0, h, q0, b);
-        tma_load_4d(sm + DO_OFF, &tm.dO, &bar_qdo, 0, h, q0, b);
-        tma_load_4d(sm + DO_OFF + BOX, &tm.dO, &bar_qdo, 64, h, q0, b);
-        tma_load_2d(sm + LSE_OFF, &tm.lse, &bar_qdo, q0, b * p.H + h);
-        tma_load_2d(sm + DLT_OFF, &tm.dlt, &bar_qdo, q0, b * p.H + h);
+        // Q_i, dO_i, LSE_i and delta_i are free once tile i-1's dK MMAs ran
+        if (t > 0 && !mbar_wait(&bar_q_free, (t - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&bar_do_full, DO_BYTES);
+        tma_load_4d(sm + DO_OFF, &tm.dO, &bar_do_full, 0, h, q0, b);
+        tma_load_4d(sm + DO_OFF + BOX, &tm.dO, &bar_do_full, 64, h, q0, b);
+        tma_load_2d(sm + LD_OFF, &tm.lse, &bar_do_full, q0, b * p.H + h);
+        tma_load_2d(sm + LD_OFF + 512, &tm.dlt, &bar_do_full, q0, b * p.H + h);
+        mbar_arrive_expect_tx(&bar_q_full, Q_BYTES);
+        tma_load_4d(sm + Q_OFF, &tm.qn, &bar_q_full, 0, h, q0, b);
+        tma_load_4d(sm + Q_OFF + BOX, &tm.qn, &bar_q_full, 64, h, q0, b);
+        tma_load_4d(sm + Q_OFF + 2 * BOX, &tm.qr, &bar_q_full, 0, h, q0, b);
       }
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idST = idesc_bf16(128, 128, 0, 0);
-      const uint32_t idDV = idesc_bf16(128, 128, 0, 1);
-      const uint32_t idDKn = idesc_bf16(128, 128, 0, 1);
+      const uint32_t idMN = idesc_bf16(128, 128, 0, 1);
       const uint32_t idDKr = idesc_bf16(128, 64, 0, 1);
       const uint32_t idDQ = idesc_bf16(128, 192, 1, 1);
       const uint32_t kb = smem_u32(sm + K_OFF), vb = smem_u32(sm + V_OFF);
-      const uint32_t qb = smem_u32(sm + Q_OFF), gb = smem_u32(sm + DO_OFF);
-      const uint32_t sb = smem_u32(sm + DS_OFF);
+      const uint32_t qb = smem_u32(sm + Q_OFF), sb = smem_u32(sm + DS_OFF);
       bool ok = mbar_wait(&bar_kv, 0, p.err);
+      const uint32_t gb = smem_u32(sm + DO_OFF);
       for (int t = 0; ok && t < n_i; ++t) {
-        if (!mbar_wait(&bar_qdo, t & 1, p.err)) break;
+        if (!mbar_wait(&bar_q_full, t & 1, p.err)) break;
+        if (!mbar_wait(&bar_do_full, t & 1, p.err)) break;
         if (t > 0 && !mbar_wait(&bar_tfree, (t - 1) & 1, p.err)) break;
         tc_fence_after();
-        // S^T = K Q^T (12 K-steps over d = 192), dP^T = V dO^T (8 over d_v)
+        // S^T = K Q^T (12 K-steps over d = 192)
 #pragma unroll
         for (int s = 0; s < 12; ++s) {
           const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
           mma_ss(tmem + C_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
                  idST, s > 0);
         }
+        mma_commit(&bar_s);
+        // dP^T = V dO^T (8 K-steps over d_v)
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
           mma_ss(tmem + C_DP, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(gb + off, 16, 1024),
                  idST, s > 0);
         }
-        mma_commit(&bar_s);
+        mma_commit(&bar_dp);
+        // dV += P^T dO (P^T from TMEM)
         if (!mbar_wait(&bar_p, t & 1, p.err)) break;
         tc_fence_after();
-        // dV += P^T dO (P^T from TMEM), dK_nope += dS^T Q_nope, dK_rope_i = dS^T Q_rope
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DV, tmem + C_S + s * 8, sdesc_sw128(gb + s * 2048, BOX, 1024), idDV,
+          mma_ts(tmem + C_DV, tmem + pt_col(s), sdesc_sw128(gb + s * 2048, BOX, 1024), idMN,
                  (t > 0 || s > 0) ? 1u : 0u);
+        // dK_nope += dS^T Q_nope, dK_rope_i = dS^T Q_rope
+        if (!mbar_wait(&bar_ds, t & 1, p.err)) break;
+        tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
           const uint64_t ad = sdesc_sw128(sb + (s >> 2) * BOX + (s & 3) * 32, 16, 1024);
-          mma_ss(tmem + C_DK, ad, sdesc_sw128(qb + s * 2048, BOX, 1024), idDKn,
+          mma_ss(tmem + C_DK, ad, sdesc_sw128(qb + s * 2048, BOX, 1024), idMN,
                  (t > 0 || s > 0) ? 1u : 0u);
         }
 #pragma unroll
@@ -177,7 +215,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint64_t ad = sdesc_sw128(sb + (s >> 2) * BOX + (s & 3) * 32, 16, 1024);
           mma_ss(tmem + C_DKR, ad, sdesc_sw128(qb + 2 * BOX + s * 2048, BOX, 1024), idDKr, s > 0);
         }
-        mma_commit(&bar_qdo_free);
+        mma_commit(&bar_q_free);
         // dQ_i = dS K (dS read MN-major from the dS^T tile, K MN-major)
 #pragma unroll
         for (int s = 0; s < 8; ++s)
@@ -187,65 +225,147 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       mma_commit(&bar_fin);
     }
-  } else if (warp < 4) {
-    // ------------------------------------------------------------- softmax
-    const int r = threadIdx.x;          // key row
+  } else {
+    // ------------------------------------------------------------- compute warps 0..7
+    const int qd = warp & 3;            // TMEM lane quadrant
+    const int ch = warp >> 2;           // column half
+    const int r = qd * 32 + lane;       // TMEM lane: key row (S^T, dP^T, dK), query row (dQ)
     const int key = k0 + r;
-    const float* lse_s = reinterpret_cast<const float*>(sm + LSE_OFF);
-    const float* dlt_s = reinterpret_cast<const float*>(sm + DLT_OFF);
     uint8_t* ds_tile = sm + DS_OFF;
+    float acc[32];                      // this thread's 32 columns of the k_pe part of dK
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
     for (int t = 0; t < n_i; ++t) {
-      const int q0 = (j + t) * BT;
+      const int i = j + t, q0 = i * BT;
+      const float* lse_s = reinterpret_cast<const float*>(sm + LD_OFF);
+      const float* dlt_s = lse_s + 128;
+      const int qlo = key - q0;         // first valid query column (causal)
+      const int qhi = p.S - q0;         // columns >= qhi are past the sequence
+      const bool key_ok = key < p.S;
+      // ---- phase A: P^T = exp2(S^T * scale * log2e - LSE * log2e)
       if (!mbar_wait(&bar_s, t & 1, p.err)) break;
       tc_fence_after();
-      // valid q columns for this key row: q >= key (causal), q < S
-      const int qlo = key - q0;          // first valid column (may be <= 0)
-      const int qhi = p.S - q0;          // columns >= qhi are past the sequence
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t us[32], ud[32];
-        tmem_ld32(tmem_addr(tmem, warp, C_S + c * 32), us);
-        tmem_ld32(tmem_addr(tmem, warp, C_DP + c * 32), ud);
-        uint32_t pk[16], dk[16];
+      float pv[64];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          float pv[2], dv[2];
+      for (int c = 0; c < 2; ++c) {
+        uint32_t us[32];
+        tmem_ld32(tmem_addr(tmem, qd, C_S + ch * 64 + c * 32), us);
+        uint32_t pk[16];
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = c * 32 + 2 * k + e;
-            const bool ok = col >= qlo && col < qhi && key < p.S;
-            const float pp =
-                ok ? exp2f(fmaf(__uint_as_float(us[2 * k + e]), p.sl2, -lse_s[col])) : 0.f;
-            pv[e] = pp;
-            dv[e] = pp * (__uint_as_float(ud[2 * k + e]) - dlt_s[col]) * p.scale;
-          }
-          pk[k] = pack_bf16(pv[0], pv[1]);
-          dk[k] = pack_bf16(dv[0], dv[1]);
+        for (int k = 0; k < 32; ++k) {
+          const int col = ch * 64 + c * 32 + k;
+          const bool ok = key_ok && col >= qlo && col < qhi;
+          pv[c * 32 + k] = ok ? ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[col])) : 0.f;
         }
-        tmem_st16(tmem_addr(tmem, warp, C_S + c * 16), pk);
-        // dS^T row r, q columns c*32 .. c*32+31 = 16-byte chunks 4c .. 4c+3
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint4 v = make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
-          *reinterpret_cast<uint4*>(ds_tile + sw_chunk_off(r, 4 * c + k)) = v;
-        }
+        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(pv[c * 32 + 2 * k], pv[c * 32 + 2 * k + 1]);
+        tmem_st16(tmem_addr(tmem, qd, C_S + ch * 64 + c * 16), pk);
       }
       tmem_wait_st();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p);
+      // ---- phase B: dS^T = P^T (dP^T - delta) * scale -> shared memory
+      if (!mbar_wait(&bar_dp, t & 1, p.err)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t ud[32];
+        tmem_ld32(tmem_addr(tmem, qd, C_DP + ch * 64 + c * 32), ud);
+        uint32_t dk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int col = ch * 64 + c * 32 + 2 * k;
+          const float d0 = pv[c * 32 + 2 * k] * (__uint_as_float(ud[2 * k]) - dlt_s[col]) * p.scale;
+          const float d1 =
+              pv[c * 32 + 2 * k + 1] * (__uint_as_float(ud[2 * k + 1]) - dlt_s[col + 1]) * p.scale;
+          dk[k] = pack_bf16(d0, d1);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint4 v = make_uint4(dk[4 * k], dk[4 * k + 1], dk[4 * k + 2], dk[4 * k + 3]);
+          *reinterpret_cast<uint4*>(ds_tile + sw_chunk_off(r, ch * 8 + c * 4 + k)) = v;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ds);
+      // ---- phase C: dQ_i and the k_pe part of dK out of TMEM
+      if (!mbar_wait(&bar_dq, t & 1, p.err)) break;
+      tc_fence_after();
+      {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tmem, qd, C_DKR + ch * 32), u);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[k] += __uint_as_float(u[k]);
+      }
+      // this thread holds dQ columns 32*(2m + ch) .. +32 for m = 0, 1, 2
+      float dqv[96];
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tmem, qd, C_DQ + 32 * (2 * m + ch)), u);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) dqv[m * 32 + k] = __uint_as_float(u[k]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_tfree);
+      // ---- ordered accumulation: key tiles add into dQ_i in order 0, 1, ..., i
+      int* sem = p.sem + ((long long)b * p.H + h) * p.n_t + i;
+      if (threadIdx.x == 0) {
+        uint32_t n = 0;
+        while (ld_acquire_gpu(sem) != j) {
+          if (++n > kSemPolls) {
+            atomicExch(p.err, DEV_ERR_TIMEOUT);
+            break;
+          }
+          if (n > 4096) __nanosleep(64);
+        }
+        fence_proxy_async_global();
+      }
+      uint8_t* stage = sm + ST_OFF + ch * BOX;
+#pragma unroll
+      for (int m = 0; m < 3; ++m) {
+        // the staging tile is free once the previous chunk's TMA has read it
+        if (m > 0 && threadIdx.x == 0) bulk_wait_read0();
+        named_bar_sync(1, N_COMPUTE * 32);
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const float4 v = make_float4(dqv[m * 32 + 4 * cc], dqv[m * 32 + 4 * cc + 1],
+                                       dqv[m * 32 + 4 * cc + 2], dqv[m * 32 + 4 * cc + 3]);
+          *reinterpret_cast<float4*>(stage + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, N_COMPUTE * 32);
+        if (threadIdx.x == 0) {
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const void* src = sm + ST_OFF + hb * BOX;
+            const int c0 = 32 * (2 * m + hb);
+            if (j == 0) tma_store_4d(&tm.dq, src, c0, h, q0, b);
+            else tma_reduce_add_4d(&tm.dq, src, c0, h, q0, b);
+          }
+          bulk_commit();
+        }
+      }
+      if (threadIdx.x == 0) {
+        bulk_wait0();                   // this tile's adds are performed ...
+        fence_proxy_async_global();
+        __threadfence();
+        st_release_gpu(sem, j + 1);     // ... before the next key tile may add
+      }
     }
-    // dK_nope, dV epilogue
+    // ---- epilogue: dK_nope (half 0) or dV (half 1) rows, k_pe part of dK
     if (mbar_wait(&bar_fin, 0, p.err)) {
       tc_fence_after();
-      __nv_bfloat16* dst = p.dkv + b * p.kv_sb + (long long)key * p.kv_ss + h * p.kv_sh;
+      __nv_bfloat16* dst = p.dkv + b * p.kv_sb + (long long)key * p.kv_ss + h * p.kv_sh + ch * 128;
+      const int src = ch == 0 ? C_DK : C_DV;
 #pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
+      for (int c = 0; c < 4; ++c) {
         uint32_t u[32];
-        // columns 0..127 of dkv <- dK_nope (TMEM 128..255); 128..255 <- dV (TMEM 0..127)
-        const int tc = c < 4 ? C_DK + c * 32 : C_DV + (c - 4) * 32;
-        tmem_ld32(tmem_addr(tmem, warp, tc), u);
+        tmem_ld32(tmem_addr(tmem, qd, src + c * 32), u);
         if (key < p.S) {
           uint4 v4[4];
           uint32_t* w = reinterpret_cast<uint32_t*>(v4);
@@ -257,74 +377,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int k = 0; k < 4; ++k) d4[k] = v4[k];
         }
       }
-    }
-  } else {
-    // ------------------------------------------------------------- dQ warps 4..7
-    const int q4 = warp & 3;
-    const int r = q4 * 32 + lane;       // TMEM lane: query row (dQ), key row (dK_rope)
-    const int key = k0 + r;
-    float acc[64];
+      if (key < p.S) {
+        float4* d4 = reinterpret_cast<float4*>(p.dkpe + (((long long)b * p.S + key) * p.H + h) * DR +
+                                               ch * 32);
 #pragma unroll
-    for (int k = 0; k < 64; ++k) acc[k] = 0.f;
-    for (int t = 0; t < n_i; ++t) {
-      const int i = j + t;
-      const int q = i * BT + r;
-      if (!mbar_wait(&bar_dq, t & 1, p.err)) break;
-      tc_fence_after();
-#pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, q4, C_DKR + c * 32), u);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) acc[c * 32 + k] += __uint_as_float(u[k]);
+        for (int k = 0; k < 8; ++k)
+          d4[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
       }
-      // wait for this (b, h, i) tile's turn: key tiles add in order 0, 1, ..., i
-      int* sem = p.sem + ((long long)b * p.H + h) * p.n_t + i;
-      if (threadIdx.x == 128) {
-        uint32_t n = 0;
-        while (ld_acquire_gpu(sem) != j) {
-          if (++n > kSpinPolls) {
-            atomicExch(p.err, DEV_ERR_TIMEOUT);
-            break;
-          }
-          if (n > 32) __nanosleep(128);
-        }
-      }
-      named_bar_sync(1, 128);
-      float* dq_row = p.dq + (((long long)b * p.S + q) * p.H + h) * DQK;
-#pragma unroll 1
-      for (int c = 0; c < 6; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, q4, C_DQ + c * 32), u);
-        if (q < p.S) {
-          float4* d4 = reinterpret_cast<float4*>(dq_row + c * 32);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            float4 v = make_float4(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
-                                   __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
-            if (j == 0) {
-              __stcg(d4 + k, v);
-            } else {
-              float4 o = __ldcg(d4 + k);
-              o.x += v.x; o.y += v.y; o.z += v.z; o.w += v.w;
-              __stcg(d4 + k, o);
-            }
-          }
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_tfree);
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (threadIdx.x == 128) st_release_gpu(sem, j + 1);
-    }
-    if (key < p.S) {
-      float* dst = p.dkpe + (((long long)b * p.S + key) * p.H + h) * DR;
-#pragma unroll
-      for (int k = 0; k < 16; ++k)
-        reinterpret_cast<float4*>(dst)[k] =
-            make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
     }
   }
   tc_fence_before();
@@ -376,6 +435,13 @@ cudaError_t launch_attn_bwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
     if ((e = make_tmap_f32(&tm.lse, x.buf<float>(p, T_LSE2), 2, dims, str, box)) != cudaSuccess)
       return e;
     if ((e = make_tmap_f32(&tm.dlt, x.buf<float>(p, T_DELTA), 2, dims, str, box)) != cudaSuccess)
+      return e;
+  }
+  {
+    // fp32 dQ accumulator [B,S,H,192]; 32-float boxes, 128-byte swizzled
+    uint64_t dims[4] = {192, H, S, B}, str[3] = {192 * 4, H * 192 * 4, S * H * 192 * 4};
+    uint32_t box[4] = {32, 1, 128, 1};
+    if ((e = make_tmap_f32(&tm.dq, x.buf<float>(p, T_DQ), 4, dims, str, box, true)) != cudaSuccess)
       return e;
   }
   BwdParams prm;

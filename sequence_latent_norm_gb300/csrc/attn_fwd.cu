@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
       mx *= p.sl2;
       const float m_new = (mx > m + RESCALE_LOG2) ? mx : m;
-      const float alpha = exp2f(m - m_new);
+      const float alpha = ex2(m - m_new);
       const bool need = j > 0 && m_new != m;
       if (__any_sync(0xffffffffu, need)) {
         // O must hold P_{j-1} V_{j-1} before it is rescaled in place.
@@ -212,8 +212,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float a = exp2f(fmaf(s[c * 32 + 2 * k], p.sl2, negm));
-          const float bb = exp2f(fmaf(s[c * 32 + 2 * k + 1], p.sl2, negm));
+          const float a = ex2(fmaf(s[c * 32 + 2 * k], p.sl2, negm));
+          const float bb = ex2(fmaf(s[c * 32 + 2 * k + 1], p.sl2, negm));
           rs += a + bb;
           pk[k] = pack_bf16(a, bb);
         }

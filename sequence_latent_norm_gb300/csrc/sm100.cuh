@@ -60,20 +60,29 @@ LAGA_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Upper bound on polls of one wait (each poll after the first few sleeps
-// ~0.5 us): a few seconds, far beyond any legitimate wait.
-constexpr uint32_t kWaitPolls = 1u << 23;
+// Upper bound on polls of one wait: the first kSpinPolls polls do not sleep
+// (try_wait itself suspends the thread briefly in hardware), later ones
+// sleep ~0.25 us each; in total a few seconds, far beyond any legitimate
+// wait.
+constexpr uint32_t kSpinPolls = 1u << 14;
+constexpr uint32_t kWaitPolls = 1u << 24;
 
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records a timeout in *err) if it never completes.
 LAGA_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
-  if (mbar_try_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (i > 16) __nanosleep(256);
+    if (i > kSpinPolls) __nanosleep(256);
   }
   if (err) atomicExch(err, DEV_ERR_TIMEOUT);
   return false;
+}
+
+// 2^x with the hardware approximation (MUFU.EX2; flushes subnormals).
+LAGA_DEVINL float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ------------------------------------------------------------------ TMA
@@ -101,6 +110,30 @@ LAGA_DEVINL void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int x, 
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
+}
+
+// TMA tensor store / reduce-add from shared memory (bulk-group completion).
+LAGA_DEVINL void tma_store_4d(const void* tmap, const void* src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+LAGA_DEVINL void tma_reduce_add_4d(const void* tmap, const void* src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.bulk_group [%0, {%2, %3, %4, %5}], "
+      "[%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+LAGA_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed bulk groups have finished reading shared memory.
+LAGA_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until the committed bulk groups have completed (writes performed).
+LAGA_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+LAGA_DEVINL void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05

@@ -48,10 +48,11 @@ inline cudaError_t make_tmap_bf16(CUtensorMap* out, const void* base, int rank,
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-// Tiled map of an fp32 tensor without swizzling (rows of up to 256 floats).
+// Tiled map of an fp32 tensor, without swizzling (rows of up to 256 floats)
+// or with 128-byte swizzling (inner box extent 32 floats).
 inline cudaError_t make_tmap_f32(CUtensorMap* out, const void* base, int rank,
                                  const uint64_t* dims, const uint64_t* strides_bytes,
-                                 const uint32_t* box) {
+                                 const uint32_t* box, bool swizzle128 = false) {
   auto enc = tmap_encoder();
   if (!enc) return cudaErrorNotSupported;
   cuuint64_t d[5], s[4];
@@ -63,7 +64,8 @@ inline cudaError_t make_tmap_f32(CUtensorMap* out, const void* base, int rank,
     if (i > 0) s[i - 1] = strides_bytes[i - 1];
   }
   CUresult r = enc(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, (cuuint32_t)rank, const_cast<void*>(base),
-                   d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
