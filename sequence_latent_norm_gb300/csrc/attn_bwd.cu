@@ -5,18 +5,22 @@
 //
 // One CTA per (128-key tile j, head h, batch b), taken from a global work
 // counter in order of increasing j (longest first); it walks the query
-// tiles i = j .. last.  10 warps:
+// tiles i = j .. last.  11 warps:
 //   warps 0-7  compute.  Warp w owns TMEM lane quadrant w%4 (key rows for
 //              S^T, dP^T, dK; query rows for dQ) and column half w/4.
 //              Phase A: S^T -> P^T (bf16 into TMEM for the TMEM-operand
 //              MMA of dV).  Phase B: dP^T -> dS^T * scale (bf16 into shared
 //              memory, 128-byte swizzled).  Phase C: copy dQ_i and this
-//              tile's k_pe part of dK out of TMEM into registers and free
-//              the columns, then add dQ_i into the fp32 dQ accumulator in
-//              global memory in a fixed order: key tile 0, 1, 2, ... through
-//              a per-(b,h,i) semaphore, so every run sums identically.  The
-//              adds are TMA tensor reduce-adds (a store for key tile 0) from
-//              a swizzled fp32 staging tile, three 64-column chunks per i.
+//              tile's k_pe part of dK out of TMEM into registers, free the
+//              columns, and write dQ_i as three 64-column fp32 chunks into
+//              128-byte-swizzled staging tiles: the staging buffer (chunks 0
+//              and 2) and the dS^T tile (chunk 1; dead between the dQ MMA and
+//              the next phase B).
+//   warp 10    dQ reducer: adds the staged chunks into the fp32 dQ
+//              accumulator in global memory with TMA tensor reduce-adds (a
+//              store for key tile 0), in a fixed order -- key tile 0, 1, 2,
+//              ... through a per-(b,h,i) semaphore -- so every run sums
+//              identically, and hands the staging tiles back.
 //   warp 8     TMA producer: K_j, V_j once; per i: Q_i, dO_i, LSE_i, delta_i.
 //   warp 9     TMEM allocator and MMA issuer.
 // TMEM columns: dV [0,128), dK_nope [128,256), S^T [256,384) with P^T in
@@ -40,17 +44,18 @@ constexpr int Q_OFF = 5 * BOX;           // Q_i: 3 boxes
 constexpr int DS_OFF = 8 * BOX;          // dS^T: 2 boxes
 constexpr int DO_OFF = 10 * BOX;         // dO_i: 2 boxes
 constexpr int ST_OFF = 12 * BOX;         // dQ staging: 2 boxes of [128 rows x 32 fp32]
+                                         // (the dS^T tile is the second staging buffer)
 constexpr int LD_OFF = 14 * BOX;         // LSE 512 B + delta 512 B
 constexpr int BAR_OFF = LD_OFF + 1024;   // mbarriers, TMEM address, work item
 constexpr int SMEM_BYTES = BAR_OFF + 256;  // 230656 B: within the 227 KiB per block
-constexpr int THREADS = 320;
+constexpr int THREADS = 352;
 constexpr int N_COMPUTE = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int C_DV = 0, C_DK = 128, C_S = 256, C_DP = 384, C_DKR = 256, C_DQ = 320;
 constexpr uint32_t KV_BYTES = 5 * BOX;
 constexpr uint32_t Q_BYTES = 3 * BOX;
 constexpr uint32_t DO_BYTES = 2 * BOX + 1024;   // dO_i + LSE_i + delta_i
-constexpr uint32_t kSemPolls = 1u << 26;
+constexpr uint32_t kSemPolls = 1u << 24;
 
 struct BwdMaps {
   CUtensorMap qn, qr, kv, kpe, dO, lse, dlt, dq;
@@ -72,6 +77,15 @@ struct BwdParams {
 // 64 columns: 16-byte chunk c (8 bf16) of the row.
 LAGA_DEVINL uint32_t sw_chunk_off(int r, int c) {
   return (uint32_t)((c >> 3) * BOX + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// Publish a key tile's TMA reduce-adds into one dQ tile: once they are
+// performed (the caller waits for their bulk groups), order them before the
+// release and hand the turn to key tile j + 1 (`next`).
+LAGA_DEVINL void release_dq(int* sem, int next) {
+  fence_proxy_async_global();
+  __threadfence();
+  st_release_gpu(sem, next);
 }
 
 // TMEM column of the P^T K-step s (16 query columns): the first 64 query
@@ -102,8 +116,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t& bar_dq = bars[11];
   uint64_t& bar_tfree = bars[12];
   uint64_t& bar_fin = bars[13];
-  uint32_t& tmem_sh = *reinterpret_cast<uint32_t*>(sm + BAR_OFF + 128);
-  int& item_sh = *reinterpret_cast<int*>(sm + BAR_OFF + 132);
+  // staged dQ chunk m is ready (8 arrivals).  One barrier per chunk: a warp
+  // may arrive for chunk m+1 before another has arrived for chunk m.
+  uint64_t* bar_stg_full = bars + 14;  // [3]
+  uint64_t& bar_a_free = bars[17];     // the staging buffer may be rewritten
+  uint64_t& bar_b_free = bars[18];     // the dS^T tile may be rewritten
+  uint32_t& tmem_sh = *reinterpret_cast<uint32_t*>(sm + BAR_OFF + 192);
+  int& item_sh = *reinterpret_cast<int*>(sm + BAR_OFF + 196);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -120,6 +139,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_dq, 1);
     mbar_init(&bar_tfree, N_COMPUTE);
     mbar_init(&bar_fin, 1);
+    for (int m = 0; m < 3; ++m) mbar_init(&bar_stg_full[m], N_COMPUTE);
+    mbar_init(&bar_a_free, 1);
+    mbar_init(&bar_b_free, 1);
     fence_barrier_init();
   }
   if (warp == 9) {
@@ -225,6 +247,52 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       mma_commit(&bar_fin);
     }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------- dQ reducer
+    if (lane == 0) {
+      for (int t = 0; t < n_i; ++t) {
+        const int i = j + t, q0 = i * BT;
+        int* sem = p.sem + ((long long)b * p.H + h) * p.n_t + i;
+        uint32_t n = 0;
+        while (ld_acquire_gpu(sem) != j) {   // key tiles add in order 0, 1, ..., i
+          if (++n > kSemPolls) {
+            atomicExch(p.err, DEV_ERR_TIMEOUT);
+            break;
+          }
+          if (n > 4096) __nanosleep(64);
+        }
+        fence_proxy_async_global();
+        bool ok = true;
+        for (int m = 0; m < 3; ++m) {
+          if (!(ok = mbar_wait(&bar_stg_full[m], t & 1, p.err))) break;
+          const int sbase = (m == 1) ? DS_OFF : ST_OFF;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const void* src = sm + sbase + hb * BOX;
+            const int c0 = 32 * (2 * m + hb);
+            if (j == 0) tma_store_4d(&tm.dq, src, c0, h, q0, b);
+            else tma_reduce_add_4d(&tm.dq, src, c0, h, q0, b);
+          }
+          bulk_commit();
+          if (m == 1) {                    // chunk 0 read: staging buffer reusable
+            bulk_wait_read1();
+            mbar_arrive(&bar_a_free);
+          }
+        }
+        bulk_wait_read0();                 // chunks 1, 2 read: both buffers reusable
+        mbar_arrive(&bar_a_free);
+        mbar_arrive(&bar_b_free);
+        if (!ok) break;
+        // the previous tile's adds have had a whole tile to land: wait for
+        // all but this tile's three bulk groups and pass that tile's turn on
+        if (t > 0) {
+          bulk_wait3();
+          release_dq(sem - 1, j + 1);
+        }
+      }
+      bulk_wait0();                        // the last tile's adds
+      release_dq(p.sem + ((long long)b * p.H + h) * p.n_t + (p.n_t - 1), j + 1);
+    }
   } else {
     // ------------------------------------------------------------- compute warps 0..7
     const int qd = warp & 3;            // TMEM lane quadrant
@@ -246,16 +314,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&bar_s, t & 1, p.err)) break;
       tc_fence_after();
       float pv[64];
+      // query tiles after the diagonal that end inside the sequence need no mask
+      const bool full = t > 0 && q0 + BT <= p.S && k0 + BT <= p.S;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t us[32];
         tmem_ld32(tmem_addr(tmem, qd, C_S + ch * 64 + c * 32), us);
         uint32_t pk[16];
+        if (full) {
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int col = ch * 64 + c * 32 + k;
-          const bool ok = key_ok && col >= qlo && col < qhi;
-          pv[c * 32 + k] = ok ? ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[col])) : 0.f;
+          for (int k = 0; k < 32; ++k)
+            pv[c * 32 + k] =
+                ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[ch * 64 + c * 32 + k]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int col = ch * 64 + c * 32 + k;
+            const bool ok = key_ok && col >= qlo && col < qhi;
+            pv[c * 32 + k] = ok ? ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[col])) : 0.f;
+          }
         }
 #pragma unroll
         for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(pv[c * 32 + 2 * k], pv[c * 32 + 2 * k + 1]);
@@ -266,6 +343,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p);
       // ---- phase B: dS^T = P^T (dP^T - delta) * scale -> shared memory
+      // (the previous tile's dQ chunk 1 was staged in the dS^T tile)
+      if (t > 0 && !mbar_wait(&bar_b_free, (t - 1) & 1, p.err)) break;
       if (!mbar_wait(&bar_dp, t & 1, p.err)) break;
       tc_fence_after();
 #pragma unroll
@@ -312,25 +391,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tfree);
-      // ---- ordered accumulation: key tiles add into dQ_i in order 0, 1, ..., i
-      int* sem = p.sem + ((long long)b * p.H + h) * p.n_t + i;
-      if (threadIdx.x == 0) {
-        uint32_t n = 0;
-        while (ld_acquire_gpu(sem) != j) {
-          if (++n > kSemPolls) {
-            atomicExch(p.err, DEV_ERR_TIMEOUT);
-            break;
-          }
-          if (n > 4096) __nanosleep(64);
-        }
-        fence_proxy_async_global();
-      }
-      uint8_t* stage = sm + ST_OFF + ch * BOX;
+      // ---- stage dQ_i for the reducer: chunks 0, 2 -> staging buffer,
+      //      chunk 1 -> dS^T tile (free: its MMAs completed with dQ_i)
 #pragma unroll
       for (int m = 0; m < 3; ++m) {
-        // the staging tile is free once the previous chunk's TMA has read it
-        if (m > 0 && threadIdx.x == 0) bulk_wait_read0();
-        named_bar_sync(1, N_COMPUTE * 32);
+        const int sbase = (m == 1) ? DS_OFF : ST_OFF;
+        if (m == 0 && t > 0 && !mbar_wait(&bar_a_free, (2 * t - 1) & 1, p.err)) break;
+        if (m == 2 && !mbar_wait(&bar_a_free, (2 * t) & 1, p.err)) break;
+        uint8_t* stage = sm + sbase + ch * BOX;
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           const float4 v = make_float4(dqv[m * 32 + 4 * cc], dqv[m * 32 + 4 * cc + 1],
@@ -338,23 +406,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           *reinterpret_cast<float4*>(stage + r * 128 + ((cc ^ (r & 7)) << 4)) = v;
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, N_COMPUTE * 32);
-        if (threadIdx.x == 0) {
-#pragma unroll
-          for (int hb = 0; hb < 2; ++hb) {
-            const void* src = sm + ST_OFF + hb * BOX;
-            const int c0 = 32 * (2 * m + hb);
-            if (j == 0) tma_store_4d(&tm.dq, src, c0, h, q0, b);
-            else tma_reduce_add_4d(&tm.dq, src, c0, h, q0, b);
-          }
-          bulk_commit();
-        }
-      }
-      if (threadIdx.x == 0) {
-        bulk_wait0();                   // this tile's adds are performed ...
-        fence_proxy_async_global();
-        __threadfence();
-        st_release_gpu(sem, j + 1);     // ... before the next key tile may add
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_stg_full[m]);
       }
     }
     // ---- epilogue: dK_nope (half 0) or dV (half 1) rows, k_pe part of dK

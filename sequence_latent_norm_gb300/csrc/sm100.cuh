@@ -65,7 +65,7 @@ LAGA_DEVINL bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // sleep ~0.25 us each; in total a few seconds, far beyond any legitimate
 // wait.
 constexpr uint32_t kSpinPolls = 1u << 14;
-constexpr uint32_t kWaitPolls = 1u << 24;
+constexpr uint32_t kWaitPolls = 1u << 22;
 
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records a timeout in *err) if it never completes.
@@ -130,6 +130,11 @@ LAGA_DEVINL void tma_reduce_add_4d(const void* tmap, const void* src, int x, int
 LAGA_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the committed bulk groups have finished reading shared memory.
 LAGA_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until all but the most recent committed bulk group have finished
+// reading shared memory.
+LAGA_DEVINL void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+// Wait until all but the three most recent bulk groups have completed.
+LAGA_DEVINL void bulk_wait3() { asm volatile("cp.async.bulk.wait_group 3;" ::: "memory"); }
 // Wait until the committed bulk groups have completed (writes performed).
 LAGA_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 LAGA_DEVINL void fence_proxy_async_global() {
