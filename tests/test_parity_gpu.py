@@ -74,6 +74,20 @@ def test_config2_full_size_sampled_heads(h):
     assert np.abs(dx.sum(-1)).max() <= 1e-3 * np.abs(dx).sum(-1).max()
 
 
+def test_emulated_sp8_matches_oracle_on_config1_dims():
+    """Emulated SP = 8 over a 16-head layer (2 heads per rank, full S): head-
+    local outputs concatenate, dc and dgamma partials sum (Section 5.2)."""
+    wl = config(1, S=1024)
+    cpu = make_inputs(wl)
+    ref = oracle_run(wl, cpu)
+    parts = [gpu_run(wl, cpu, heads=(2 * r, 2)) for r in range(8)]
+    sp = dict(O=torch.cat([p["O"] for p in parts], 2), LSE=torch.cat([p["LSE"] for p in parts], 1),
+              dq=torch.cat([p["dq"] for p in parts], 2), dw=torch.cat([p["dw"] for p in parts], 1),
+              dc=sum(p["dc"] for p in parts), dgamma=sum(p["dgamma"] for p in parts))
+    check_forward(sp, ref, "sp8")
+    check_grads(sp, ref, where="sp8")
+
+
 def test_run_to_run_bitwise_determinism():
     wl = config(1, S=1000, H=4)
     cpu = make_inputs(wl)
@@ -83,10 +97,20 @@ def test_run_to_run_bitwise_determinism():
 
 
 def test_laga_equals_explicit_form_bitwise_at_sp1():
-    """Proposition 1 / Section 4.5: same matmuls, reordered K/V views."""
-    wl = config(3, S=1024)
+    """Proposition 1 / Section 4.5: same matmuls, reordered K/V views.
+    Full-head SP=1 run (S=4096, n_h=128); both forms also against the oracle
+    on sampled heads."""
+    wl = config(3)
     cpu = make_inputs(wl)
     a = gpu_run(wl, cpu, form="laga")
     b = gpu_run(wl, cpu, form="explicit")
     for k in a:
         assert torch.equal(a[k], b[k]), k
+    for h in (0, 77):
+        ref = oracle_run(wl, cpu, heads=[h])
+        check_forward(dict(O=a["O"][:, :, h], LSE=a["LSE"][:, h]),
+                      dict(O=ref["O"][:, :, h], LSE=ref["LSE"][:, h], vmax=ref["vmax"][:, :, h]),
+                      f"config3 head {h}")
+        assert rel_fro(as_f64(a["dq"][:, :, h]), ref["dq"][:, :, h]) <= GRAD_REL_FRO
+        cols = dw_cols(wl, h)
+        assert rel_fro(as_f64(a["dw"][:, cols]), ref["dw"][:, cols]) <= GRAD_REL_FRO
