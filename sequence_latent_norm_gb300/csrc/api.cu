@@ -150,7 +150,7 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
   Plan p;
   laga_status s = make_plan(dims, &p);
   if (s != LAGA_OK) return s;
-  if (p.d.form == LAGA_FORM_ABSORBED) return LAGA_ERR_UNSUPPORTED;
+  const bool absorbed = p.d.form == LAGA_FORM_ABSORBED;
   const void* ptrs[] = {q, c, w_kvb, gamma, cos, sin, o, lse, ws_saved};
   for (const void* ptr : ptrs)
     if (!ptr) return LAGA_ERR_ARG;
@@ -166,8 +166,12 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
   cudaError_t e = cudaSuccess;
   if (!p.canonical) e = launch_pad_w(p, x, st);
   if (e == cudaSuccess) e = launch_prep_fwd(p, x, st);
-  if (e == cudaSuccess) e = launch_upproj(p, x, st);
-  if (e == cudaSuccess) e = launch_attn_fwd(p, x, st);
+  if (absorbed) {
+    if (e == cudaSuccess) e = launch_absorbed_fwd(p, x, st);
+  } else {
+    if (e == cudaSuccess) e = launch_upproj(p, x, st);
+    if (e == cudaSuccess) e = launch_attn_fwd(p, x, st);
+  }
   if (e == cudaSuccess && !p.canonical) e = launch_unpad_o(p, x, st);
   return cuda_status(e);
 }
@@ -181,7 +185,7 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
   Plan p;
   laga_status s = make_plan(dims, &p);
   if (s != LAGA_OK) return s;
-  if (p.d.form == LAGA_FORM_ABSORBED) return LAGA_ERR_UNSUPPORTED;
+  const bool absorbed = p.d.form == LAGA_FORM_ABSORBED;
   const void* ptrs[] = {q, c, w_kvb, gamma, cos, sin, o, lse, d_o, dq, dc, dw, dgamma,
                         ws_saved, ws_bwd};
   for (const void* ptr : ptrs)
@@ -198,9 +202,14 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
   if ((s = err_word(&x.err)) != LAGA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_bwd_pre(p, x, st);
-  if (e == cudaSuccess) e = launch_attn_bwd(p, x, st);
-  if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
-  if (e == cudaSuccess) e = launch_upproj_bwd(p, x, st);
+  if (absorbed) {
+    if (e == cudaSuccess) e = launch_absorbed_bwd(p, x, st);
+    if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
+  } else {
+    if (e == cudaSuccess) e = launch_attn_bwd(p, x, st);
+    if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
+    if (e == cudaSuccess) e = launch_upproj_bwd(p, x, st);
+  }
   if (e == cudaSuccess && !p.canonical) e = launch_unpad_dw(p, x, st);
   if (e == cudaSuccess) e = launch_norm_bwd(p, x, x.buf<float>(p, T_DL), st);
   return cuda_status(e);

@@ -57,7 +57,11 @@ cudaError_t launch_unpad_dw(const Plan& p, const Ptrs& x, cudaStream_t st);
 cudaError_t launch_upproj(const Plan& p, const Ptrs& x, cudaStream_t st);
 cudaError_t launch_upproj_bwd(const Plan& p, const Ptrs& x, cudaStream_t st);
 
-// attn.cu: causal attention forward and backward.
+// absorbed.cu: the absorbed-form contrast path (attention over the latent).
+cudaError_t launch_absorbed_fwd(const Plan& p, const Ptrs& x, cudaStream_t st);
+cudaError_t launch_absorbed_bwd(const Plan& p, const Ptrs& x, cudaStream_t st);
+
+// attn_fwd.cu / attn_bwd.cu: causal attention forward and backward.
 cudaError_t launch_attn_fwd(const Plan& p, const Ptrs& x, cudaStream_t st);
 cudaError_t launch_attn_bwd(const Plan& p, const Ptrs& x, cudaStream_t st);
 

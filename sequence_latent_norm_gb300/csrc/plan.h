@@ -36,8 +36,8 @@ enum BufId {
   T_DGP,        // fp32 [NGP, 512]      dgamma partial sums
   T_DWC,        // fp32 [512, H*256]    padded dW shard
   T_DOLAT,      // bf16 [B*S*H, 512]    dO up-projected to the latent (absorbed)
-  T_DQABS,      // bf16 [B*S*H, 512]    gradient of q_absorbed (absorbed)
-  T_DLF,        // fp32 [B*S, 512]      attention part of dL (absorbed)
+  T_DQABS,      // fp32 [B*S*H, 512]    gradient of q_absorbed (absorbed)
+  T_DLF,        // (unused)
   T_DWP,        // fp32 [splits, 512, H*256] split-K partials of dW
   T_SEM,        // int  [B*H*ceil(S/128) + 1] ordered-dQ semaphores + work counter
   N_BUF
@@ -122,18 +122,17 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
   p->len[T_LSE2] = (size_t)p->B * H * p->s_pad() * 4;
   if (!p->canonical) p->len[T_DOC] = R * 128 * 2;
   p->len[T_DQ] = R * 192 * 4;
-  p->len[T_DKV] = R * 256 * 2;
+  if (!absorbed) p->len[T_DKV] = R * 256 * 2;
   p->len[T_DKPE] = R * 64 * 4;
   p->len[T_DL] = T * 512 * 4;
   p->len[T_DGP] = (size_t)NGP * 512 * 4;
   if (!p->canonical) p->len[T_DWC] = (size_t)512 * H * 256 * 4;
   if (absorbed) {
     p->len[T_DOLAT] = R * 512 * 2;
-    p->len[T_DQABS] = R * 512 * 2;
-    p->len[T_DLF] = T * 512 * 4;
+    p->len[T_DQABS] = R * 512 * 4;
   }
   p->len[T_SEM] = ((size_t)p->B * p->H * ((p->S + 127) / 128) + 1) * 4;
-  if (dw_splits(p->H) > 1) p->len[T_DWP] = (size_t)dw_splits(p->H) * 512 * H * 256 * 4;
+  if (!absorbed && dw_splits(p->H) > 1) p->len[T_DWP] = (size_t)dw_splits(p->H) * 512 * H * 256 * 4;
   size_t o = 0;
   for (int i = 0; i < N_SAVED; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }
   p->saved_bytes = o;
