@@ -48,6 +48,15 @@ def parse_args():
     ap.add_argument("--config", type=int, default=2, help="workload configuration (default 2)")
     ap.add_argument("--form", default="laga", choices=["laga", "explicit"])
     ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--seq", type=int, default=0,
+                    help="override the sequence length (smaller cases for profiling)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="sequence/head sweep of LAGA and the absorbed form: throughput and "
+                         "measured activation memory against the closed form (one JSON line "
+                         "per point)")
+    ap.add_argument("--sweep-S", default="2048,4096,8192,16384,32768")
+    ap.add_argument("--sweep-H", default="8,16,32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -233,6 +242,38 @@ def max_over_ranks(value: float, world: int, device=None) -> float:
     return float(t.item())
 
 
+# ----------------------------------------------------------------- end to end
+def end_to_end(args, cpu, dev, stream, step, flush, outs, world, attn_flops):
+    """The same metric through the public API with host buffers: every step
+    copies the step's inputs from pinned host memory to the device, runs the
+    forward and backward, and copies every output back to pinned host memory,
+    all inside the timed region."""
+    import torch
+    host_in = {k: v.pin_memory() for k, v in cpu.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
+    d2h = sum(x.numel() * x.element_size() for x in outs)
+    dev_in = {k: torch.empty_like(v, device=dev) for k, v in cpu.items()}
+    times = []
+    for i in range(args.e2e_steps + 1):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        a.record(stream)
+        for k in dev_in:
+            dev_in[k].copy_(host_in[k], non_blocking=True)
+        step(dev_in)
+        for x, hx in zip(outs, host_out):
+            hx.copy_(x, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        if i > 0:                       # the first pass warms the pinned copies
+            times.append(a.elapsed_time(b))
+    ms = statistics.mean(times)
+    return {"value": round(world * attn_flops / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms, 3)}
+
+
 # ----------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import dataclasses
@@ -243,7 +284,7 @@ def run_ours(args, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    base = config(args.config)
+    base = config(args.config, **({"S": args.seq} if args.seq else {}))
     wl = rank_workload(base, rank, world)
     S, H, B = wl.S, wl.H, wl.B
 
@@ -325,28 +366,10 @@ def run_ours(args, rank, world, local_rank):
     value = world * attn_flops / (ms_per_step * 1e-3) / 1e12
 
     # ---- end to end through the public API with host buffers
-    host_in = {k: v.pin_memory() for k, v in cpu.items()}
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    outs = [o, lse, dq, dc, dw, dg]
-    host_out = [torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in outs]
-    d2h = sum(x.numel() * x.element_size() for x in outs)
-    dev_in = {k: torch.empty_like(v, device=dev) for k, v in cpu.items()}
-    e2e_ms = []
-    for i in range(args.e2e_steps + 1):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize(dev)
-        a.record(stream)
-        for k in dev_in:
-            dev_in[k].copy_(host_in[k], non_blocking=True)
-        step(dev_in)
-        for x, hx in zip(outs, host_out):
-            hx.copy_(x, non_blocking=True)
-        b.record(stream)
-        torch.cuda.synchronize(dev)
-        if i > 0:
-            e2e_ms.append(a.elapsed_time(b))
-    e2e_val = world * attn_flops / (statistics.mean(e2e_ms) * 1e-3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(args, cpu, dev, stream, step, flush, [o, lse, dq, dc, dw, dg], world,
+                         attn_flops)
 
     # ---- per-kernel rates and the roofline of the dominant kernel
     peak_tf, peak_gbs, peak_src = measured_peaks()
@@ -391,16 +414,71 @@ def run_ours(args, rank, world, local_rank):
             "block_tflops": round((attn_flops + up_f) / (ms_per_step * 1e-3) / 1e12, 2),
             "wall_s_timed": round(t_wall, 3),
             "clocks": clk,
-            "e2e": {"value": round(e2e_val, 3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(statistics.mean(e2e_ms), 3)},
+            "e2e": e2e,
             "gpu_launches": launches[0] * args.steps,
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu_baseline}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------- sweep
+def run_sweep(args):
+    """S x H grid for the LAGA and absorbed forms (DeepSeek-V3 dims, bf16):
+    fwd+bwd time, attention TFLOP/s, and the measured peak device memory of a
+    forward (saved activations + outputs) against the per-token closed form
+    (absorbed: q_absorbed and the latent accumulator, n_h*d_kv each; LAGA:
+    per-head K/V, n_h*(d_nope+d_v))."""
+    import torch
+    import sequence_latent_norm_gb300 as pkg
+    from laga_inputs import config, make_inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    for S in [int(x) for x in args.sweep_S.split(",")]:
+        for H in [int(x) for x in args.sweep_H.split(",")]:
+            wl = config(4, S=S, H=H, n_h_total=H)
+            cpu = make_inputs(wl)
+            t = {k: v.to(dev) for k, v in cpu.items()}
+            peak = {}
+            for form in ("laga", "absorbed"):
+                torch.cuda.synchronize(dev)
+                torch.cuda.empty_cache()
+                torch.cuda.reset_peak_memory_stats(dev)
+                base = torch.cuda.memory_allocated(dev)
+                run = pkg.Laga(pkg.Shard(S=S, H=H, form=form), device=dev)
+                o, lse = run.forward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"])
+                torch.cuda.synchronize(dev)
+                peak[form] = torch.cuda.max_memory_allocated(dev) - base
+                times = []
+                for it in range(2):
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record()
+                    o, lse = run.forward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"], o, lse)
+                    run.backward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"], o, lse, t["dO"])
+                    b.record()
+                    torch.cuda.synchronize(dev)
+                    times.append(a.elapsed_time(b))
+                pkg._lib.sync_check()
+                ms = times[-1]
+                f, bw = attention_flops(S, H)
+                line = {"sweep": "config4", "form": form, "S": S, "H": H, "ms_fwd_bwd": round(ms, 3),
+                        "attn_tflops": round((f + bw) / (ms * 1e-3) / 1e12, 2),
+                        "peak_fwd_bytes": peak[form],
+                        "saved_workspace_bytes": run.saved_bytes}
+                if form == "absorbed":
+                    per_tok = (2 * H * 512 - H * 256) * 2
+                    line["measured_gap_bytes"] = peak["absorbed"] - peak["laga"]
+                    line["closed_form_gap_bytes"] = S * per_tok
+                    line["gap_ratio"] = round(line["measured_gap_bytes"] / line["closed_form_gap_bytes"], 4)
+                print(json.dumps(line), flush=True)
+                del run, o, lse
+                torch.cuda.empty_cache()
+
+
 def main():
     args = parse_args()
+    if args.sweep:
+        run_sweep(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
