@@ -2,23 +2,28 @@
 // (Algorithm 1 step 5: scores = (q_nope||q_rope)(k_nope||k_pe)^T / sqrt(d),
 // out = softmax(scores) v; Section 5.3: k_pe shared by all heads).
 //
-// One CTA per (128-row query tile, head, batch), 6 warps:
-//   warps 0-3  softmax: thread r owns query row r (TMEM lane r).  Reads the
-//              score row S_j from TMEM, applies the causal mask on the
-//              diagonal tile, keeps the running max m (base-2 domain) and
-//              sum l, writes P_j = exp2(s*scale*log2e - m) as bf16 back into
-//              the same TMEM columns, and rescales the O accumulator only
-//              when its row max grows by more than 2^8 (the result is exact
-//              either way: O and l carry the same stale max).
-//   warp 4     TMA producer: Q once (q_nope | RoPE'd q_rope, 3 boxes), then
-//              per key tile K_j (k_nope | k_pe, 3 boxes) and V_j (2 boxes)
-//              into two-stage rings.
-//   warp 5     TMEM allocator and MMA issuer: S_{j+1} = Q K_{j+1}^T (12
-//              K-steps, the two column bands are consecutive K chunks of the
-//              same accumulator) is issued before O += P_j V_j (8 K-steps, P
-//              from TMEM), so the tensor core works on the next tile while
-//              the softmax warps handle this one.
-// TMEM columns: S/P double buffer [0,256), O [256,384).
+// One CTA per (128-row query tile, head, batch), 11 warps:
+//   warps 0-7  softmax: warp w owns query rows 32*(w%4) .. +32 (TMEM lanes)
+//              and key-column half w/4 of every score tile.  A thread reads
+//              its 64 scores of S_j from TMEM, applies the causal mask on
+//              the diagonal tile, takes the row max together with the
+//              partner warp that holds the other half of the row (through
+//              shared memory and an mbarrier), keeps the running max m
+//              (base-2 domain) and its half of the sum l, writes
+//              P_j = exp2(s*scale*log2e - m) as bf16 back into its own
+//              TMEM columns, and rescales its half of the O accumulator only
+//              when the row max grows by more than 2^8 (exact either way: O
+//              and l carry the same stale max).
+//   warp 8     TMA producer of Q once (q_nope | RoPE'd q_rope, 3 boxes) and
+//              per key tile K_j (k_nope | k_pe, 3 boxes) into a two-stage
+//              ring; warp 10 the same for V_j (2 boxes).
+//   warp 9     TMEM allocator and MMA issuer: S_{j+1} = Q K_{j+1}^T (12
+//              K-steps) is issued before O += P_j V_j (8 K-steps, P from
+//              TMEM), so the tensor core works on the next tile while the
+//              softmax warps handle this one.
+// TMEM columns: S/P double buffer [0,256) (P of key columns 0-63 packed into
+// the first 32 columns of a buffer, of 64-127 into columns 64-95), O
+// [256,384).
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -35,7 +40,9 @@ constexpr int Q_BYTES = 3 * BOX;
 constexpr int K_BYTES = 3 * BOX;
 constexpr int V_BYTES = 2 * BOX;
 constexpr int SMEM_BYTES = Q_BYTES + 2 * (K_BYTES + V_BYTES) + 1024;
-constexpr int THREADS = 192;
+constexpr int THREADS = 352;
+constexpr int N_SOFTMAX = 8;
+constexpr int W_PROD = 8, W_MMA = 9, W_VPROD = 10;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int O_COL = 256;
 constexpr float RESCALE_LOG2 = 8.0f;
@@ -60,7 +67,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* Qs = sm;
   uint8_t* Ks = sm + Q_BYTES;
   uint8_t* Vs = Ks + 2 * K_BYTES;
-  __shared__ uint64_t bar_q, bar_kf[2], bar_ke[2], bar_vf[2], bar_ve[2], bar_s[2], bar_p[2], bar_o;
+  // bar_s[st]: S_j in TMEM, which also means K stage st has been read;
+  // bar_ve[st]: P_j V_j done, so V stage st and S buffer st are free and O
+  // holds every product up to tile j
+  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_ve[2], bar_s[2], bar_p[2];
+  // row-max exchange between the two warps of a query-row quadrant, per S
+  // buffer; the final row-sum exchange
+  __shared__ uint64_t bar_mx[4][2], bar_lx[4];
+  __shared__ float red_mx[2][2][BM], red_l[2][BM];
   __shared__ uint32_t tmem_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -75,16 +89,19 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_q, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_kf[i], 1);
-      mbar_init(&bar_ke[i], 1);
       mbar_init(&bar_vf[i], 1);
       mbar_init(&bar_ve[i], 1);
       mbar_init(&bar_s[i], 1);
-      mbar_init(&bar_p[i], 4);
+      mbar_init(&bar_p[i], N_SOFTMAX);
     }
-    mbar_init(&bar_o, 1);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(&bar_mx[q][0], 2);
+      mbar_init(&bar_mx[q][1], 2);
+      mbar_init(&bar_lx[q], 2);
+    }
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tmem_alloc(&tmem_sh, TMEM_COLS);
     tmem_relinquish();
   }
@@ -93,7 +110,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
 
-  if (warp == 4) {
+  if (warp == W_PROD) {
+    // Q, then K_j into its ring stage as soon as S_{j-2} has read it
     if (lane == 0) {
       tma_prefetch_desc(&tm.qn);
       tma_prefetch_desc(&tm.kv);
@@ -104,20 +122,28 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; j < n_kt; ++j) {
         const int st = j & 1;
         const int k0 = j * BN;
-        if (j >= 2 && !mbar_wait(&bar_ke[st], ((j >> 1) - 1) & 1, p.err)) break;
+        if (j >= 2 && !mbar_wait(&bar_s[st], ((j >> 1) - 1) & 1, p.err)) break;
         uint8_t* kd = Ks + st * K_BYTES;
         mbar_arrive_expect_tx(&bar_kf[st], K_BYTES);
         tma_load_4d(kd, &tm.kv, &bar_kf[st], 0, k0, h, b);
         tma_load_4d(kd + BOX, &tm.kv, &bar_kf[st], 64, k0, h, b);
         tma_load_3d(kd + 2 * BOX, &tm.kpe, &bar_kf[st], 0, k0, b);
+      }
+    }
+  } else if (warp == W_VPROD) {
+    // V_j into its ring stage as soon as P_{j-2} V_{j-2} has read it (its
+    // own warp, so a late V stage never holds back the next K load)
+    if (lane == 0) {
+      for (int j = 0; j < n_kt; ++j) {
+        const int st = j & 1;
         if (j >= 2 && !mbar_wait(&bar_ve[st], ((j >> 1) - 1) & 1, p.err)) break;
         uint8_t* vd = Vs + st * V_BYTES;
         mbar_arrive_expect_tx(&bar_vf[st], V_BYTES);
-        tma_load_4d(vd, &tm.kv, &bar_vf[st], 128, k0, h, b);
-        tma_load_4d(vd + BOX, &tm.kv, &bar_vf[st], 192, k0, h, b);
+        tma_load_4d(vd, &tm.kv, &bar_vf[st], 128, j * BN, h, b);
+        tma_load_4d(vd + BOX, &tm.kv, &bar_vf[st], 192, j * BN, h, b);
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == W_MMA) {
     if (lane == 0) {
       const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idO = idesc_bf16(BM, 128, 0, 1);
@@ -135,7 +161,6 @@ __global__ void __launch_bounds__(THREADS, 1)
           mma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS, s > 0);
         }
         mma_commit(&bar_s[st]);
-        mma_commit(&bar_ke[st]);
         return true;
       };
       if (ok) ok = issue_s(0);
@@ -149,66 +174,74 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t pa = tmem + st * BN;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + O_COL, pa + s * 8, sdesc_sw128(va + s * 2048, BOX, 1024), idO,
+          mma_ts(tmem + O_COL, pa + (s < 4 ? 8 * s : 64 + 8 * (s - 4)),
+                 sdesc_sw128(va + s * 2048, BOX, 1024), idO,
                  (j > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_ve[st]);
-        mma_commit(&bar_o);
       }
     }
   } else {
     // ---------------------------------------------------------- softmax warps
-    const int r = threadIdx.x;
+    const int qd = warp & 3;            // TMEM lane quadrant = query rows
+    const int ch = warp >> 2;           // key-column half
+    const int r = qd * 32 + lane;
     const int qi = q0 + r;
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY, l = 0.f;       // l: this half's part of the row sum
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
       const int st = j & 1;
       if (!mbar_wait(&bar_s[st], (j >> 1) & 1, p.err)) { ok = false; break; }
       tc_fence_after();
-      float s[BN];
+      float s[64];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, warp, st * BN + c * 32), u);
+        tmem_ld32(tmem_addr(tmem, qd, st * BN + ch * 64 + c * 32), u);
 #pragma unroll
         for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(u[k]);
       }
       if (j == n_kt - 1) {  // diagonal tile: key k0+c visible iff c <= r and k0+c < S
-        const int lim = min(r, p.S - 1 - j * BN);
+        const int lim = min(r, p.S - 1 - j * BN) - ch * 64;
 #pragma unroll
-        for (int c = 0; c < BN; ++c)
+        for (int c = 0; c < 64; ++c)
           if (c > lim) s[c] = -INFINITY;
       }
       float mx = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < BN; ++c) mx = fmaxf(mx, s[c]);
-      mx *= p.sl2;
+      for (int c = 0; c < 64; ++c) mx = fmaxf(mx, s[c]);
+      // row max over both halves
+      red_mx[st][ch][r] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_mx[qd][st]);
+      if (!mbar_wait(&bar_mx[qd][st], (j >> 1) & 1, p.err)) { ok = false; break; }
+      mx = fmaxf(mx, red_mx[st][ch ^ 1][r]) * p.sl2;
       const float m_new = (mx > m + RESCALE_LOG2) ? mx : m;
       const float alpha = ex2(m - m_new);
       const bool need = j > 0 && m_new != m;
       if (__any_sync(0xffffffffu, need)) {
         // O must hold P_{j-1} V_{j-1} before it is rescaled in place.
-        if (!mbar_wait(&bar_o, (j - 1) & 1, p.err)) { ok = false; break; }
+        if (!mbar_wait(&bar_ve[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
+          const int col = O_COL + ch * 64 + c * 32;
           uint32_t u[32];
-          tmem_ld32(tmem_addr(tmem, warp, O_COL + c * 32), u);
+          tmem_ld32(tmem_addr(tmem, qd, col), u);
           uint32_t lo[16], hi[16];
 #pragma unroll
           for (int k = 0; k < 16; ++k) {
             lo[k] = __float_as_uint(__uint_as_float(u[k]) * alpha);
             hi[k] = __float_as_uint(__uint_as_float(u[16 + k]) * alpha);
           }
-          tmem_st16(tmem_addr(tmem, warp, O_COL + c * 32), lo);
-          tmem_st16(tmem_addr(tmem, warp, O_COL + c * 32 + 16), hi);
+          tmem_st16(tmem_addr(tmem, qd, col), lo);
+          tmem_st16(tmem_addr(tmem, qd, col + 16), hi);
         }
       }
       m = m_new;
       float rs = 0.f;
       const float negm = -m;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
@@ -217,7 +250,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           rs += a + bb;
           pk[k] = pack_bf16(a, bb);
         }
-        tmem_st16(tmem_addr(tmem, warp, st * BN + c * 16), pk);
+        // P of this half packed into the first 32 of its own 64 S columns
+        tmem_st16(tmem_addr(tmem, qd, st * BN + ch * 64 + c * 16), pk);
       }
       l = l * alpha + rs;
       tmem_wait_st();
@@ -226,18 +260,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (lane == 0) mbar_arrive(&bar_p[st]);
     }
     // ---------------------------------------------------------- epilogue
-    // A parity wait is exact only if the barrier is at most one phase behind
-    // the awaited one.  The last S tile seen here guarantees only P V up to
-    // tile n_kt-3, so wait for tile n_kt-2 before tile n_kt-1.
-    if (ok && n_kt >= 2) ok = mbar_wait(&bar_o, (n_kt - 2) & 1, p.err);
-    if (ok && mbar_wait(&bar_o, (n_kt - 1) & 1, p.err)) {
+    // O is complete once P V of the last tile is done (each stage barrier
+    // is waited for its own latest phase, so the parity test is exact)
+    if (ok && n_kt >= 2) ok = mbar_wait(&bar_ve[(n_kt - 2) & 1], ((n_kt - 2) >> 1) & 1, p.err);
+    if (ok) ok = mbar_wait(&bar_ve[(n_kt - 1) & 1], ((n_kt - 1) >> 1) & 1, p.err);
+    if (ok) {
+      red_l[ch][r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_lx[qd]);
+      ok = mbar_wait(&bar_lx[qd], 0, p.err);
+    }
+    if (ok) {
       tc_fence_after();
-      const float inv = 1.0f / l;
-      __nv_bfloat16* orow = p.O + (((long long)b * p.S + qi) * p.H + h) * 128;
+      const float lt = l + red_l[ch ^ 1][r];
+      const float inv = 1.0f / lt;
+      __nv_bfloat16* orow = p.O + (((long long)b * p.S + qi) * p.H + h) * 128 + ch * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, warp, O_COL + c * 32), u);
+        tmem_ld32(tmem_addr(tmem, qd, O_COL + ch * 64 + c * 32), u);
         uint4 v4[4];
         uint32_t* w = reinterpret_cast<uint32_t*>(v4);
 #pragma unroll
@@ -249,12 +290,12 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int k = 0; k < 4; ++k) dst[k] = v4[k];
         }
       }
-      if (qi < p.S) p.lse[((long long)b * p.H + h) * p.S + qi] = (m + log2f(l)) * LN2;
+      if (ch == 0 && qi < p.S) p.lse[((long long)b * p.H + h) * p.S + qi] = (m + log2f(lt)) * LN2;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }

@@ -70,6 +70,10 @@ constexpr uint32_t kWaitPolls = 1u << 22;
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records a timeout in *err) if it never completes.
 LAGA_DEVINL bool mbar_wait(uint64_t* bar, uint32_t parity, int* err) {
+  // Phase already complete: one probe, no loop (the common case on the
+  // issue paths, where a few hundred cycles per wait show up as tensor-core
+  // idle time).
+  if (mbar_try_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < kWaitPolls; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (i > kSpinPolls) __nanosleep(256);
