@@ -279,9 +279,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_arrive(&bar_a_free);
           }
         }
-        bulk_wait_read0();                 // chunks 1, 2 read: both buffers reusable
-        mbar_arrive(&bar_a_free);
+        bulk_wait_read1();                 // chunk 1 read: the dS^T tile is free
         mbar_arrive(&bar_b_free);
+        bulk_wait_read0();                 // chunk 2 read: the staging buffer is free
+        mbar_arrive(&bar_a_free);
         if (!ok) break;
         // the previous tile's adds have had a whole tile to land: wait for
         // all but this tile's three bulk groups and pass that tile's turn on
