@@ -263,6 +263,261 @@ __global__ void __launch_bounds__(256) unpad_dw_kernel(const float* __restrict__
   }
 }
 
+// ---------------------------------------------------------------------------
+// Canonical dims (d_kv 512, d_rope 64, d_nope = d_v = 128) with bf16 I/O:
+// the same steps with 16-byte accesses.  A lane owns eight consecutive
+// elements (one 16-byte chunk); the rotate-half partner of chunk c is c + 4.
+
+LAGA_DEVINL void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 t = __bfloat1622float2(h[k]);
+    f[2 * k] = t.x;
+    f[2 * k + 1] = t.y;
+  }
+}
+LAGA_DEVINL uint4 f32x8_to_bf16(const float (&f)[8]) {
+  uint4 v;
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+    w[k] = *reinterpret_cast<uint32_t*>(&t);
+  }
+  return v;
+}
+LAGA_DEVINL void load_f32x8(const float* p, float (&f)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w;
+  f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+}
+
+// Rotate the pair (chunk c, chunk c+4) of a 64-wide band by position s:
+// x'[i] = x[i] cos - x[i+32] sin, x'[i+32] = x[i+32] cos + x[i] sin.
+LAGA_DEVINL void rope_chunk_pair(const __nv_bfloat16* src, __nv_bfloat16* dst, int c,
+                                 const float* cs_row, const float* sn_row) {
+  float a[8], b[8], cs[8], sn[8];
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + 8 * c), a);
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(src + 32 + 8 * c), b);
+  load_f32x8(cs_row + 8 * c, cs);
+  load_f32x8(sn_row + 8 * c, sn);
+  float x[8], y[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    x[k] = a[k] * cs[k] - b[k] * sn[k];
+    y[k] = b[k] * cs[k] + a[k] * sn[k];
+  }
+  *reinterpret_cast<uint4*>(dst + 8 * c) = f32x8_to_bf16(x);
+  *reinterpret_cast<uint4*>(dst + 32 + 8 * c) = f32x8_to_bf16(y);
+}
+
+// a1 + a2, one warp per token.
+__global__ void __launch_bounds__(256) prep_fwd_v_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ c,
+    const float* __restrict__ gamma, const float* __restrict__ cosT,
+    const float* __restrict__ sinT, int S, int H, long long tokens, float eps,
+    __nv_bfloat16* __restrict__ L, float* __restrict__ mean_o, float* __restrict__ rstd_o,
+    __nv_bfloat16* __restrict__ kpe, __nv_bfloat16* __restrict__ qr) {
+  const int lane = threadIdx.x & 31;
+  const long long tok = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
+  if (tok >= tokens) return;
+  const int s = (int)(tok % S);
+  const __nv_bfloat16* crow = c + tok * 576;
+  float x[2][8];
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(crow + 8 * lane), x[0]);
+  bf16x8_to_f32(*reinterpret_cast<const uint4*>(crow + 256 + 8 * lane), x[1]);
+  float sum = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) sum += x[0][k] + x[1][k];
+  const float mu = warp_sum(sum) * (1.0f / 512);
+  float sq = 0.f;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float d0 = x[0][k] - mu, d1 = x[1][k] - mu;
+    sq += d0 * d0 + d1 * d1;
+  }
+  const float rstd = 1.0f / sqrtf(warp_sum(sq) * (1.0f / 512) + eps);
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    const int col = 256 * hh + 8 * lane;
+    float g[8], y[8];
+    load_f32x8(gamma + col, g);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) y[k] = (x[hh][k] - mu) * rstd * g[k];
+    *reinterpret_cast<uint4*>(L + tok * 512 + col) = f32x8_to_bf16(y);
+  }
+  if (lane == 0) { mean_o[tok] = mu; rstd_o[tok] = rstd; }
+  const float* cs_row = cosT + (long long)s * 32;
+  const float* sn_row = sinT + (long long)s * 32;
+  if (lane < 4) rope_chunk_pair(crow + 512, kpe + tok * 64, lane, cs_row, sn_row);
+  // every head's q_rope: 4 chunk pairs per head
+  for (int task = lane; task < 4 * H; task += 32) {
+    const int h = task >> 2, cc = task & 3;
+    const long long row = tok * H + h;
+    rope_chunk_pair(q + row * 192 + 128, qr + row * 64, cc, cs_row, sn_row);
+  }
+}
+
+// delta = rowsum(dO * O): a half-warp per (token, head) row of 128.
+__global__ void __launch_bounds__(256) bwd_pre_v_kernel(
+    const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ d_o, int S, int H,
+    long long rows, float* __restrict__ delta, int* __restrict__ sem, int n_sem,
+    const float* __restrict__ lse, float* __restrict__ lse2, int s_pad) {
+  for (int i = blockIdx.x * 256 + threadIdx.x; i < n_sem; i += gridDim.x * 256) sem[i] = 0;
+  const int sub = threadIdx.x & 15;
+  const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
+  const bool ok = row < rows;
+  float acc = 0.f;
+  if (ok) {
+    float a[8], g[8];
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(o + row * 128 + 8 * sub), a);
+    bf16x8_to_f32(*reinterpret_cast<const uint4*>(d_o + row * 128 + 8 * sub), g);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc += a[k] * g[k];
+  }
+#pragma unroll
+  for (int m = 8; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (ok && sub == 0) {
+    const int h = (int)(row % H);
+    const long long tok = row / H;
+    const int b = (int)(tok / S), s = (int)(tok % S);
+    const long long pr = ((long long)b * H + h) * s_pad + s;
+    delta[pr] = acc;
+    lse2[pr] = lse[((long long)b * H + h) * S + s] * 1.4426950408889634f;
+  }
+}
+
+// dq in the raw frame: the nope band cast, the rope band rotated back (R^T).
+// A warp takes DQ_ROWS rows and issues all of their loads before any store.
+constexpr int DQ_ROWS = 4;
+__global__ void __launch_bounds__(256) dq_final_v_kernel(const float* __restrict__ dqr, int S,
+                                                         int H, long long rows,
+                                                         const float* __restrict__ cosT,
+                                                         const float* __restrict__ sinT,
+                                                         __nv_bfloat16* __restrict__ dq) {
+  const int lane = threadIdx.x & 31;
+  const long long row0 = ((long long)blockIdx.x * WARPS + (threadIdx.x >> 5)) * DQ_ROWS;
+  float4 nope[DQ_ROWS];
+  float a[DQ_ROWS], b[DQ_ROWS], cs[DQ_ROWS], sn[DQ_ROWS];
+#pragma unroll
+  for (int k = 0; k < DQ_ROWS; ++k) {
+    const long long row = row0 + k;
+    if (row < rows) {
+      const float* src = dqr + row * 192;
+      const int s = (int)((row / H) % S);
+      nope[k] = *reinterpret_cast<const float4*>(src + 4 * lane);
+      a[k] = src[128 + lane];
+      b[k] = src[160 + lane];
+      cs[k] = cosT[(long long)s * 32 + lane];
+      sn[k] = sinT[(long long)s * 32 + lane];
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < DQ_ROWS; ++k) {
+    const long long row = row0 + k;
+    if (row < rows) {
+      __nv_bfloat16* dst = dq + row * 192;
+      __nv_bfloat162 lo = __floats2bfloat162_rn(nope[k].x, nope[k].y);
+      __nv_bfloat162 hi = __floats2bfloat162_rn(nope[k].z, nope[k].w);
+      uint2 w;
+      w.x = *reinterpret_cast<uint32_t*>(&lo);
+      w.y = *reinterpret_cast<uint32_t*>(&hi);
+      *reinterpret_cast<uint2*>(dst + 4 * lane) = w;
+      dst[128 + lane] = __float2bfloat16_rn(a[k] * cs[k] + b[k] * sn[k]);
+      dst[160 + lane] = __float2bfloat16_rn(b[k] * cs[k] - a[k] * sn[k]);
+    }
+  }
+}
+
+// a7, one warp per token; a lane owns latent columns 8*lane.. and
+// 256 + 8*lane.., and the k_pe column pair (2*lane, 2*lane+1) of the sum
+// over heads (taken in head order).
+__global__ void __launch_bounds__(256) norm_bwd_v_kernel(
+    const float* __restrict__ dL, const __nv_bfloat16* __restrict__ c,
+    const float* __restrict__ mean, const float* __restrict__ rstd,
+    const float* __restrict__ gamma, const float* __restrict__ dkpe_h,
+    const float* __restrict__ cosT, const float* __restrict__ sinT, int S, int H,
+    long long tokens, float* __restrict__ dc, float* __restrict__ dg_part) {
+  __shared__ float red[WARPS][512];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float gm[2][8], dg[2][8];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh) {
+    load_f32x8(gamma + 256 * hh + 8 * lane, gm[hh]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dg[hh][k] = 0.f;
+  }
+  for (long long tok = (long long)blockIdx.x * WARPS + warp; tok < tokens;
+       tok += (long long)gridDim.x * WARPS) {
+    const __nv_bfloat16* crow = c + tok * 576;
+    const float mu = mean[tok], rs = rstd[tok];
+    float xh[2][8], g[2][8];
+    float s1 = 0.f, s2 = 0.f;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int col = 256 * hh + 8 * lane;
+      float xv[8], d[8];
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(crow + col), xv);
+      load_f32x8(dL + tok * 512 + col, d);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        xh[hh][k] = (xv[k] - mu) * rs;
+        g[hh][k] = d[k] * gm[hh][k];
+        dg[hh][k] += d[k] * xh[hh][k];
+        s1 += g[hh][k];
+        s2 += g[hh][k] * xh[hh][k];
+      }
+    }
+    const float m1 = warp_sum(s1) * (1.0f / 512), m2 = warp_sum(s2) * (1.0f / 512);
+    float* drow = dc + tok * 576;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      float r[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) r[k] = rs * (g[hh][k] - m1 - xh[hh][k] * m2);
+      float* dst = drow + 256 * hh + 8 * lane;
+      *reinterpret_cast<float4*>(dst) = make_float4(r[0], r[1], r[2], r[3]);
+      *reinterpret_cast<float4*>(dst + 4) = make_float4(r[4], r[5], r[6], r[7]);
+    }
+    // sum over heads of the per-head k_pe gradient, columns 2*lane, 2*lane+1
+    float2 a = make_float2(0.f, 0.f);
+    for (int h = 0; h < H; ++h) {
+      const float2 v = *reinterpret_cast<const float2*>(dkpe_h + (tok * H + h) * 64 + 2 * lane);
+      a.x += v.x;
+      a.y += v.y;
+    }
+    // rotate back: lanes < 16 hold x[i], lanes >= 16 hold x[i + 32]
+    float2 pb;
+    pb.x = __shfl_xor_sync(0xffffffffu, a.x, 16);
+    pb.y = __shfl_xor_sync(0xffffffffu, a.y, 16);
+    const int s = (int)(tok % S), i = 2 * (lane & 15);
+    const float2 cs = *reinterpret_cast<const float2*>(cosT + (long long)s * 32 + i);
+    const float2 sn = *reinterpret_cast<const float2*>(sinT + (long long)s * 32 + i);
+    float2 out;
+    if (lane < 16) {
+      out.x = a.x * cs.x + pb.x * sn.x;
+      out.y = a.y * cs.y + pb.y * sn.y;
+    } else {
+      out.x = a.x * cs.x - pb.x * sn.x;
+      out.y = a.y * cs.y - pb.y * sn.y;
+    }
+    *reinterpret_cast<float2*>(drow + 512 + 2 * lane) = out;
+  }
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) red[warp][256 * hh + 8 * lane + k] = dg[hh][k];
+  __syncthreads();
+  for (int col = threadIdx.x; col < 512; col += 256) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) t += red[w][col];
+    dg_part[(long long)blockIdx.x * 512 + col] = t;
+  }
+}
+
 inline int grid_for(long long n, int per_block) {
   long long g = (n + per_block - 1) / per_block;
   return (int)(g < 1 ? 1 : g);
@@ -297,7 +552,11 @@ cudaError_t launch_prep_fwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
   auto* qr = x.buf<__nv_bfloat16>(p, W_QR);
   float* mean = x.buf<float>(p, W_MEAN);
   float* rstd = x.buf<float>(p, W_RSTD);
-  if (p.fp32)
+  if (p.canonical)
+    prep_fwd_v_kernel<<<g, 256, 0, st>>>((const __nv_bfloat16*)x.q, (const __nv_bfloat16*)x.c,
+                                         x.gamma, x.cos, x.sin, p.S, p.H, p.tokens(), p.d.ln_eps,
+                                         L, mean, rstd, kpe, qr);
+  else if (p.fp32)
     prep_fwd_kernel<float><<<g, 256, 0, st>>>((const float*)x.q, (const float*)x.c, x.gamma, x.cos,
                                               x.sin, p.B, p.S, p.H, p.dn, p.dr, p.dkv, p.d.ln_eps,
                                               L, mean, rstd, kpe, qr, qn);
@@ -327,7 +586,11 @@ cudaError_t launch_bwd_pre(const Plan& p, const Ptrs& x, cudaStream_t st) {
   int* sem = x.buf<int>(p, T_SEM);
   float* lse2 = x.buf<float>(p, T_LSE2);
   const int n_sem = (int)(p.len[T_SEM] / 4);
-  if (p.fp32)
+  if (p.canonical)
+    bwd_pre_v_kernel<<<grid_for(p.rows(), 16), 256, 0, st>>>(
+        (const __nv_bfloat16*)x.o, (const __nv_bfloat16*)x.d_o, p.S, p.H, p.rows(), delta, sem,
+        n_sem, x.lse, lse2, (int)p.s_pad());
+  else if (p.fp32)
     bwd_pre_kernel<float><<<g, 256, 0, st>>>((const float*)x.o, (const float*)x.d_o, p.B, p.S, p.H,
                                              p.dv, delta, dop, sem, n_sem, x.lse, lse2,
                                              (int)p.s_pad());
@@ -343,7 +606,10 @@ cudaError_t launch_dq_finalize(const Plan& p, const Ptrs& x, cudaStream_t st) {
   LaunchScope ls_("dq_final", st);
   const int g = grid_for(p.rows(), WARPS);
   const float* dqr = x.buf<float>(p, T_DQ);
-  if (p.fp32)
+  if (p.canonical)
+    dq_final_v_kernel<<<grid_for(p.rows(), WARPS * DQ_ROWS), 256, 0, st>>>(
+        dqr, p.S, p.H, p.rows(), x.cos, x.sin, (__nv_bfloat16*)x.dq);
+  else if (p.fp32)
     dq_final_kernel<float><<<g, 256, 0, st>>>(dqr, p.B, p.S, p.H, p.dn, p.dr, x.cos, x.sin,
                                               (float*)x.dq);
   else
@@ -357,7 +623,11 @@ cudaError_t launch_norm_bwd(const Plan& p, const Ptrs& x, const float* dL, cudaS
   float* part = x.buf<float>(p, T_DGP);
   {
   LaunchScope ls_("norm_bwd", st);
-  if (p.fp32)
+  if (p.canonical)
+    norm_bwd_v_kernel<<<NGP, 256, 0, st>>>(dL, (const __nv_bfloat16*)x.c, x.buf<float>(p, W_MEAN),
+                                           x.buf<float>(p, W_RSTD), x.gamma, dk, x.cos, x.sin, p.S,
+                                           p.H, p.tokens(), x.dc, part);
+  else if (p.fp32)
     norm_bwd_kernel<float><<<NGP, 256, 0, st>>>(dL, (const float*)x.c, x.buf<float>(p, W_MEAN),
                                                 x.buf<float>(p, W_RSTD), x.gamma, dk, x.cos, x.sin,
                                                 p.B, p.S, p.H, p.dr, p.dkv, x.dc, part);
