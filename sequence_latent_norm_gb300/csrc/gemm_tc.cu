@@ -21,7 +21,7 @@ namespace laga {
 namespace {
 using namespace sm100;
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 2;   // two CTAs per SM
 constexpr int A_BYTES = BM * BK * 2;   // 16 KB
 constexpr int B_BYTES = BN * BK * 2;   // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -69,7 +69,7 @@ LAGA_DEVINL void load_stage(const GemmMaps& tm, uint8_t* a_dst, uint8_t* b_dst, 
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(THREADS, 1)
+__global__ void __launch_bounds__(THREADS, 2)
     gemm_tc_kernel(const __grid_constant__ GemmMaps tm, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
