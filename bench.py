@@ -176,21 +176,21 @@ def attention_flops(S, H, B=1):
 
 
 # ----------------------------------------------------------------- CPU oracle
-def oracle_sample(wl, S_sample: int, head: int = 0):
-    """Time the fp64 oracle's fwd+bwd of one head of the workload on the
+def oracle_sample(wl, S_sample: int, heads: int = 1):
+    """Time the fp64 oracle's fwd+bwd of `heads` heads of the workload on the
     first S_sample tokens; returns (seconds, attention FLOPs of the sample)."""
     import dataclasses
     import oracle
     from laga_inputs import as_f64, make_inputs
-    sub = dataclasses.replace(wl, S=S_sample, H=1, n_h_total=1, head_offset=0)
+    sub = dataclasses.replace(wl, S=S_sample, H=heads, n_h_total=heads, head_offset=0)
     cpu = make_inputs(sub)
     a = {k: as_f64(v) for k, v in cpu.items()}
-    d = oracle.Dims(S=sub.S, H=1)
+    d = oracle.Dims(S=sub.S, H=heads)
     t0 = time.perf_counter()
     _, _, st = oracle.forward(a["q"], a["c"], a["w"], a["gamma"], a["cos"], a["sin"], d)
     oracle.backward(st, a["dO"])
     dt = time.perf_counter() - t0
-    f, b = attention_flops(S_sample, 1)
+    f, b = attention_flops(S_sample, heads)
     return dt, f + b
 
 
@@ -317,10 +317,11 @@ def run_ours(args, rank, world, local_rank):
     # CPU baseline first (rank 0, one GPU only): the oracle as it stands.
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        dt, fl = oracle_sample(base, base.S)
+        nh = min(4, base.H)
+        dt, fl = oracle_sample(base, base.S, nh)
         cpu_baseline = {"value": fl / dt / 1e12, "unit": UNIT, "cores": os.cpu_count(),
                         "kind": "oracle",
-                        "sample": f"fp64 NumPy oracle fwd+bwd of 1 of the {H} heads over all "
+                        "sample": f"fp64 NumPy oracle fwd+bwd of {nh} of the {H} heads over all "
                                   f"{S} tokens ({dt:.1f} s)"}
 
     cpu = make_inputs(wl)
