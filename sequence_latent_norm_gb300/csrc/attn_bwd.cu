@@ -284,15 +284,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         bulk_wait_read0();                 // chunk 2 read: the staging buffer is free
         mbar_arrive(&bar_a_free);
         if (!ok) break;
-        // the previous tile's adds have had a whole tile to land: wait for
-        // all but this tile's three bulk groups and pass that tile's turn on
-        if (t > 0) {
-          bulk_wait3();
-          release_dq(sem - 1, j + 1);
-        }
+        // pass the turn on as soon as this tile's adds are performed: the
+        // next key tile's CTA is usually already waiting for it
+        bulk_wait0();
+        release_dq(sem, j + 1);
       }
-      bulk_wait0();                        // the last tile's adds
-      release_dq(p.sem + ((long long)b * p.H + h) * p.n_t + (p.n_t - 1), j + 1);
     }
   } else {
     // ------------------------------------------------------------- compute warps 0..7

@@ -137,8 +137,6 @@ LAGA_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read
 // Wait until all but the most recent committed bulk group have finished
 // reading shared memory.
 LAGA_DEVINL void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-// Wait until all but the three most recent bulk groups have completed.
-LAGA_DEVINL void bulk_wait3() { asm volatile("cp.async.bulk.wait_group 3;" ::: "memory"); }
 // Wait until the committed bulk groups have completed (writes performed).
 LAGA_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 LAGA_DEVINL void fence_proxy_async_global() {
