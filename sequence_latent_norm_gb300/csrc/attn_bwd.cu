@@ -5,7 +5,7 @@
 //
 // One CTA per (128-key tile j, head h, batch b), taken from a global work
 // counter in order of increasing j (longest first); it walks the query
-// tiles i = j .. last.  11 warps:
+// tiles i = last .. j.  11 warps:
 //   warps 0-7  compute.  Warp w owns TMEM lane quadrant w%4 (key rows for
 //              S^T, dP^T, dK; query rows for dQ) and column half w/4.
 //              Phase A: S^T -> P^T (bf16 into TMEM for the TMEM-operand
@@ -158,7 +158,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int h = (item % per) % p.H;
   const int b = (item % per) / p.H;
   const int k0 = j * BT;
-  const int n_i = p.n_t - j;   // query tiles j .. n_t-1
+  // query tiles last .. j, the diagonal last: a CTA started later reaches
+  // every tile after the CTAs of lower key tiles started before it, which is
+  // the order the dQ adds must take
+  const int n_i = p.n_t - j;
 
   if (warp == 8) {
     // ------------------------------------------------------------- producer
@@ -170,7 +173,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tma_load_4d(sm + V_OFF, &tm.kv, &bar_kv, 128, k0, h, b);
       tma_load_4d(sm + V_OFF + BOX, &tm.kv, &bar_kv, 192, k0, h, b);
       for (int t = 0; t < n_i; ++t) {
-        const int q0 = (j + t) * BT;
+        const int q0 = (p.n_t - 1 - t) * BT;
         // Q_i, dO_i, LSE_i and delta_i are free once tile i-1's dK MMAs ran
         if (t > 0 && !mbar_wait(&bar_q_free, (t - 1) & 1, p.err)) break;
         mbar_arrive_expect_tx(&bar_do_full, DO_BYTES);
@@ -251,7 +254,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ------------------------------------------------------------- dQ reducer
     if (lane == 0) {
       for (int t = 0; t < n_i; ++t) {
-        const int i = j + t, q0 = i * BT;
+        const int i = p.n_t - 1 - t, q0 = i * BT;
         int* sem = p.sem + ((long long)b * p.H + h) * p.n_t + i;
         uint32_t n = 0;
         while (ld_acquire_gpu(sem) != j) {   // key tiles add in order 0, 1, ..., i
@@ -301,7 +304,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
     for (int k = 0; k < 32; ++k) acc[k] = 0.f;
     for (int t = 0; t < n_i; ++t) {
-      const int i = j + t, q0 = i * BT;
+      const int i = p.n_t - 1 - t, q0 = i * BT;
       const float* lse_s = reinterpret_cast<const float*>(sm + LD_OFF);
       const float* dlt_s = lse_s + 128;
       const int qlo = key - q0;         // first valid query column (causal)
@@ -312,7 +315,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       float pv[64];
       // query tiles after the diagonal that end inside the sequence need no mask
-      const bool full = t > 0 && q0 + BT <= p.S && k0 + BT <= p.S;
+      const bool full = i > j && q0 + BT <= p.S && k0 + BT <= p.S;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t us[32];
