@@ -144,6 +144,13 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
  * up since the last check on this device (and clear the flag). */
 laga_status laga_sync_check(void* stream);
 
+/* Diagnostic of the error path above; the paper has no counterpart.
+ * Enqueues one single-thread kernel whose bounded wait (about 17 ms) on an
+ * mbarrier that nothing arrives on gives up, so the next laga_sync_check()
+ * on this device reports LAGA_ERR_TIMEOUT.  No fault, no unbounded spin.
+ * Returns LAGA_ERR_CUDA if the launch fails. */
+laga_status laga_selftest_wait_timeout(void* stream);
+
 /* Static text for a status code. */
 const char* laga_status_string(laga_status status);
 

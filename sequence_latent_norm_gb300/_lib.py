@@ -23,7 +23,7 @@ WS_SAVED, WS_BWD = 0, 1
 EXPORTED = ("laga_workspace_bytes", "laga_workspace_tensor", "laga_fwd", "laga_bwd",
             "laga_sync_check", "laga_status_string", "laga_last_launch_count",
             "laga_profile_enable", "laga_profile_reset", "laga_profile_read",
-            "laga_norm_rope_bwd_noalloc")
+            "laga_norm_rope_bwd_noalloc", "laga_selftest_wait_timeout")
 
 
 class LagaDims(ctypes.Structure):
@@ -65,6 +65,8 @@ def load(path: str = LIB_PATH):
     lib.laga_bwd.restype = I
     lib.laga_sync_check.argtypes = [P]
     lib.laga_sync_check.restype = I
+    lib.laga_selftest_wait_timeout.argtypes = [P]
+    lib.laga_selftest_wait_timeout.restype = I
     lib.laga_status_string.argtypes = [I]
     lib.laga_status_string.restype = ctypes.c_char_p
     lib.laga_last_launch_count.argtypes = []
@@ -130,6 +132,11 @@ def bwd(dims: LagaDims, q, c, w, gamma, cos, sin, o, lse, d_o, dq, dc, dw, dgamm
 
 def sync_check(stream=0):
     _check(load().laga_sync_check(stream), "laga_sync_check")
+
+
+def selftest_wait_timeout(stream=0):
+    """Enqueue the bounded-wait self-test (see include/laga.h)."""
+    _check(load().laga_selftest_wait_timeout(stream), "laga_selftest_wait_timeout")
 
 
 def last_launch_count() -> int:

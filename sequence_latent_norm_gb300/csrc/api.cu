@@ -7,6 +7,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "sm100.cuh"
 
 namespace laga {
 
@@ -111,6 +112,21 @@ Views make_views(const Plan& p, const Ptrs& x) {
 
 using namespace laga;
 
+// One thread waits, with a short bound (2^16 polls, ~17 ms), on an mbarrier
+// that nothing arrives on, then records the timeout code in the device error
+// word -- the same path every kernel's bounded waits take.
+static __global__ void selftest_wait_timeout_kernel(int* err) {
+  __shared__ uint64_t bar;
+  laga::sm100::mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  for (uint32_t i = 0; i < (1u << 16); ++i) {
+    if (laga::sm100::mbar_try_wait(&bar, 0)) return;
+    __nanosleep(256);
+  }
+  atomicExch(err, laga::DEV_ERR_TIMEOUT);
+}
+
+
 extern "C" {
 
 size_t laga_workspace_bytes(const laga_dims* dims, int pass) {
@@ -213,6 +229,14 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
   if (e == cudaSuccess && !p.canonical) e = launch_unpad_dw(p, x, st);
   if (e == cudaSuccess) e = launch_norm_bwd(p, x, x.buf<float>(p, T_DL), st);
   return cuda_status(e);
+}
+
+laga_status laga_selftest_wait_timeout(void* stream) {
+  int* w = nullptr;
+  laga_status s = err_word(&w);
+  if (s != LAGA_OK) return s;
+  selftest_wait_timeout_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(w);
+  return cudaGetLastError() == cudaSuccess ? LAGA_OK : LAGA_ERR_CUDA;
 }
 
 laga_status laga_sync_check(void* stream) {

@@ -114,3 +114,17 @@ def test_laga_equals_explicit_form_bitwise_at_sp1():
         assert rel_fro(as_f64(a["dq"][:, :, h]), ref["dq"][:, :, h]) <= GRAD_REL_FRO
         cols = dw_cols(wl, h)
         assert rel_fro(as_f64(a["dw"][:, cols]), ref["dw"][:, cols]) <= GRAD_REL_FRO
+
+
+def test_laga_equals_explicit_form_bitwise_on_ragged_batch():
+    """The identity of the two forms on a ragged length, B = 2 and a shard
+    inside a wider W_kv_b, and both against the oracle."""
+    wl = config(1, S=333, H=3, B=2, n_h_total=7, head_offset=2)
+    cpu = make_inputs(wl)
+    a = gpu_run(wl, cpu, form="laga")
+    b = gpu_run(wl, cpu, form="explicit")
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+    ref = oracle_run(wl, cpu)
+    check_forward(a, ref, "ragged laga")
+    check_grads(a, ref, where="ragged laga")
