@@ -1,0 +1,430 @@
+// a5, key-stationary half of the causal MLA attention backward: dK and dV
+// (Section 5.2).  With P = exp(s - LSE), delta = rowsum(dO * O):
+//   dV = P^T dO,  dP^T = V dO^T,  dS^T = P^T (dP^T - delta) * scale,
+//   dK = dS^T Q   (the k_pe band of dK kept per head).
+// dQ = dS K is the query-stationary kernel's (attn_bwd_dq.cu); with no dQ
+// here, neither P^T nor dS^T ever leaves TMEM and nothing is reduced across
+// CTAs, so every output element is one fixed-order accumulation.
+//
+// One CTA per (128-key tile j, head h, batch b), longest (smallest j)
+// first; it walks the query tiles i = j .. last.  12 warps:
+//   warps 0-7  compute.  Warp w owns TMEM lane quadrant w%4 (key rows) and
+//              column half w/4 (query columns).  Phase A: S^T -> P^T (bf16
+//              packed into its own S^T columns, the TMEM operand of dV).
+//              Phase B: dP^T -> dS^T * scale (bf16 packed into its own dP^T
+//              columns, the TMEM operand of dK).  Then it adds this tile's
+//              k_pe part of dK from TMEM into registers.
+//   warp 8     TMA producer: K_j, V_j once; per i: Q_i with LSE_i and
+//              delta_i (double-buffered), dO_i.
+//   warp 9     TMEM allocator and MMA issuer.  Per i: dP^T_i, dV, then
+//              S^T_{i+1} (so the next tile's scores overlap phase B), dK.
+//   warps 10-11 idle (they complete warpgroup 2 for the register split).
+// TMEM columns: dV [0,128), dK_nope [128,256), S^T [256,384) with P^T in
+// [256,288) and [320,352), dP^T [384,512) with dS^T in [384,416) and
+// [480,512); the k_pe part of dK for tile i goes to [416,480), the dP^T
+// columns phase B has read and left free.  Every mbarrier is waited phase
+// by phase, so parity waits are exact.
+#include "common.cuh"
+#include "kernels.h"
+#include "sm100.cuh"
+#include "tmap.h"
+
+namespace laga {
+namespace {
+using namespace sm100;
+
+constexpr int BT = 128;                  // key tile = query tile
+constexpr int BOX = 128 * 64 * 2;        // 16 KB
+constexpr int K_OFF = 0;                 // K_j: 3 boxes (k_nope | k_pe)
+constexpr int V_OFF = 3 * BOX;           // V_j: 2 boxes
+constexpr int Q_OFF = 5 * BOX;           // Q_i: two buffers of 3 boxes
+constexpr int DO_OFF = 11 * BOX;         // dO_i: 2 boxes
+constexpr int LD_OFF = 13 * BOX;         // 2 x (LSE 512 B + delta 512 B)
+constexpr int SMEM_BYTES = LD_OFF + 2048 + 1024;   // + slack to align the base
+constexpr int THREADS = 384;   // 12 warps: 3 whole warpgroups for setmaxnreg
+constexpr int N_COMPUTE = 8;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int C_DV = 0, C_DK = 128, C_S = 256, C_DP = 384, C_DKR = C_DP + 32;
+constexpr uint32_t KV_BYTES = 5 * BOX;
+constexpr uint32_t Q_BYTES = 3 * BOX + 1024;    // Q_i + LSE_i + delta_i
+constexpr uint32_t DO_BYTES = 2 * BOX;
+
+struct KvMaps {
+  CUtensorMap qn, qr, kv, kpe, dO, lse, dlt;
+};
+struct KvParams {
+  int S, H, B, n_t;
+  float sl2;                 // scale * log2(e)
+  float scale;
+  __nv_bfloat16* dkv;        // per-head [.., 256]
+  long long kv_sb, kv_ss, kv_sh;
+  float* dkpe;               // [R, 64]
+  int* err;
+};
+
+// TMEM column of the K-step s (16 query columns) of the packed P^T tile:
+// query columns 0-63 are packed into [C_S, C_S+32), 64-127 into
+// [C_S+64, C_S+96).
+LAGA_DEVINL uint32_t pt_col(int s) { return s < 4 ? C_S + 8 * s : C_S + 64 + 8 * (s - 4); }
+// The same for the packed dS^T tile, at the two ends of the dP^T columns,
+// [C_DP, C_DP+32) and [C_DP+96, C_DP+128), which leaves [C_DP+32, C_DP+96)
+// for the k_pe part of dK.
+LAGA_DEVINL uint32_t dst_col(int s) { return s < 4 ? C_DP + 8 * s : C_DP + 96 + 8 * (s - 4); }
+
+// Phase B on the 32 query columns [32C, 32C+32) of this warp's half: read
+// dP^T from `rd` + 32C, write dS^T = P^T (dP^T - delta) * scale as 16 packed
+// bf16 pairs to `wr` + 16C.
+template <int C>
+LAGA_DEVINL void ds_chunk(uint32_t rd, uint32_t wr, const float (&pv)[64], const float* dlt,
+                          float scale) {
+  uint32_t ud[32], dk[16];
+  tmem_ld32(rd + C * 32, ud);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float2 dl = reinterpret_cast<const float2*>(dlt + C * 32)[k];
+    const float d0 = pv[C * 32 + 2 * k] * (__uint_as_float(ud[2 * k]) - dl.x) * scale;
+    const float d1 = pv[C * 32 + 2 * k + 1] * (__uint_as_float(ud[2 * k + 1]) - dl.y) * scale;
+    dk[k] = pack_bf16(d0, d1);
+  }
+  tmem_st16(wr + C * 16, dk);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    attn_bwd_kv_kernel(const __grid_constant__ KvMaps tm, const KvParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  __shared__ uint64_t bar_kv, bar_q_full[2], bar_q_free[2], bar_do_full, bar_do_free;
+  __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_dkr, bar_tfree, bar_fin;
+  __shared__ uint32_t tmem_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bar_kv, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bar_q_full[k], 1);
+      mbar_init(&bar_q_free[k], 1);
+    }
+    mbar_init(&bar_do_full, 1);
+    mbar_init(&bar_do_free, 1);
+    mbar_init(&bar_s, 1);
+    mbar_init(&bar_dp, 1);
+    mbar_init(&bar_p, N_COMPUTE);
+    mbar_init(&bar_ds, N_COMPUTE);
+    mbar_init(&bar_dkr, 1);
+    mbar_init(&bar_tfree, N_COMPUTE);
+    mbar_init(&bar_fin, 1);
+    fence_barrier_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(&tmem_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_sh;
+  const int per = p.H * p.B;
+  const int j = (int)(blockIdx.x / per);   // smallest key tiles (longest walks) first
+  const int h = (int)(blockIdx.x % per) % p.H;
+  const int b = (int)(blockIdx.x % per) / p.H;
+  const int k0 = j * BT;
+  const int n_i = p.n_t - j;              // query tiles j .. n_t-1
+  // 168 registers a thread at launch (10 warps): warps 8-9 give back 112
+  // each, the compute warps take 24 each, 8*32*192 + 2*32*56 <= 320*168
+
+  // 168 registers a thread at launch (12 warps).  Warpgroup 2 (producer,
+  // MMA issuer, two idle warps) drops to 72, the compute warps rise to 200:
+  // 8*32*200 + 4*32*72 = 60416 <= 384*168, and 200+200+72 per SMSP.
+  if (warp >= 8) {
+  reg_shrink<72>();
+  if (warp == 8) {
+    // ------------------------------------------------------------- producer
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bar_kv, KV_BYTES);
+      tma_load_4d(sm + K_OFF, &tm.kv, &bar_kv, 0, k0, h, b);
+      tma_load_4d(sm + K_OFF + BOX, &tm.kv, &bar_kv, 64, k0, h, b);
+      tma_load_3d(sm + K_OFF + 2 * BOX, &tm.kpe, &bar_kv, 0, k0, b);
+      tma_load_4d(sm + V_OFF, &tm.kv, &bar_kv, 128, k0, h, b);
+      tma_load_4d(sm + V_OFF + BOX, &tm.kv, &bar_kv, 192, k0, h, b);
+      for (int t = 0; t < n_i; ++t) {
+        const int q0 = (j + t) * BT;
+        const int qb = t & 1;
+        // Q_i, LSE_i, delta_i into buffer i%2 once the dK MMAs of tile i-2
+        // have read it (phase B of i-2 has read LSE and delta before those)
+        if (t >= 2 && !mbar_wait(&bar_q_free[qb], ((t >> 1) - 1) & 1, p.err)) break;
+        uint8_t* qd = sm + Q_OFF + qb * 3 * BOX;
+        uint8_t* ld = sm + LD_OFF + qb * 1024;
+        mbar_arrive_expect_tx(&bar_q_full[qb], Q_BYTES);
+        tma_load_4d(qd, &tm.qn, &bar_q_full[qb], 0, h, q0, b);
+        tma_load_4d(qd + BOX, &tm.qn, &bar_q_full[qb], 64, h, q0, b);
+        tma_load_4d(qd + 2 * BOX, &tm.qr, &bar_q_full[qb], 0, h, q0, b);
+        tma_load_2d(ld, &tm.lse, &bar_q_full[qb], q0, b * p.H + h);
+        tma_load_2d(ld + 512, &tm.dlt, &bar_q_full[qb], q0, b * p.H + h);
+        // dO_i once dV_{i-1} has read dO_{i-1}
+        if (t > 0 && !mbar_wait(&bar_do_free, (t - 1) & 1, p.err)) break;
+        mbar_arrive_expect_tx(&bar_do_full, DO_BYTES);
+        tma_load_4d(sm + DO_OFF, &tm.dO, &bar_do_full, 0, h, q0, b);
+        tma_load_4d(sm + DO_OFF + BOX, &tm.dO, &bar_do_full, 64, h, q0, b);
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t idST = idesc_bf16(128, 128, 0, 0);
+      const uint32_t idMN = idesc_bf16(128, 128, 0, 1);
+      const uint32_t idDKr = idesc_bf16(128, 64, 0, 1);
+      const uint32_t kb = smem_u32(sm + K_OFF), vb = smem_u32(sm + V_OFF);
+      const uint32_t gb = smem_u32(sm + DO_OFF);
+      // S^T_i = K Q_i^T (12 K-steps over d = 192) into [256,384)
+      auto issue_s = [&](int t) -> bool {
+        if (!mbar_wait(&bar_q_full[t & 1], (t >> 1) & 1, p.err)) return false;
+        tc_fence_after();
+        const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
+#pragma unroll
+        for (int s = 0; s < 12; ++s) {
+          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
+          mma_ss(tmem + C_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
+                 idST, s > 0);
+        }
+        mma_commit(&bar_s);
+        return true;
+      };
+      bool ok = mbar_wait(&bar_kv, 0, p.err) && issue_s(0);
+      for (int t = 0; ok && t < n_i; ++t) {
+        const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
+        // dP^T = V dO^T (8 K-steps over d_v) into [384,512): dS^T of tile
+        // i-1 there was read by the dK MMAs issued before, and the k_pe part
+        // of dK of tile i-1 has been read out once tfree completes
+        if (!mbar_wait(&bar_do_full, t & 1, p.err)) break;
+        if (t > 0 && !mbar_wait(&bar_tfree, (t - 1) & 1, p.err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
+          mma_ss(tmem + C_DP, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(gb + off, 16, 1024),
+                 idST, s > 0);
+        }
+        mma_commit(&bar_dp);
+        // dV += P^T dO (P^T from TMEM); afterwards dO_i is no longer read
+        if (!mbar_wait(&bar_p, t & 1, p.err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ts(tmem + C_DV, tmem + pt_col(s), sdesc_sw128(gb + s * 2048, BOX, 1024), idMN,
+                 (t > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&bar_do_free);
+        // S^T_{i+1} overwrites P^T_i only after the dV MMAs above read it
+        if (t + 1 < n_i && !issue_s(t + 1)) break;
+        // dK_rope_i = dS^T Q_rope into [416,480), dK_nope += dS^T Q_nope
+        if (!mbar_wait(&bar_ds, t & 1, p.err)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ts(tmem + C_DKR, tmem + dst_col(s), sdesc_sw128(qb + 2 * BOX + s * 2048, BOX, 1024),
+                 idDKr, s > 0);
+        mma_commit(&bar_dkr);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_ts(tmem + C_DK, tmem + dst_col(s), sdesc_sw128(qb + s * 2048, BOX, 1024), idMN,
+                 (t > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&bar_q_free[t & 1]);
+      }
+      mma_commit(&bar_fin);
+    }
+  }
+  } else {
+  reg_grow<200>();
+    // ------------------------------------------------------------- compute warps 0..7
+    const int qd = warp & 3;            // TMEM lane quadrant
+    const int ch = warp >> 2;           // column half
+    const int r = qd * 32 + lane;       // TMEM lane: key row
+    const int key = k0 + r;
+    const bool key_ok = key < p.S;
+    float acc[32];                      // this thread's 32 columns of the k_pe part of dK
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+    for (int t = 0; t < n_i; ++t) {
+      const int i = j + t, q0 = i * BT;
+      const float* lse_s = reinterpret_cast<const float*>(sm + LD_OFF + (t & 1) * 1024);
+      const float* dlt_s = lse_s + 128;
+      const int qlo = key - q0;         // first valid query column (causal)
+      const int qhi = p.S - q0;         // columns >= qhi are past the sequence
+      // ---- phase A: P^T = exp2(S^T * scale * log2e - LSE * log2e)
+      if (!mbar_wait(&bar_q_full[t & 1], (t >> 1) & 1, p.err)) break;   // LSE_i, delta_i
+      if (!mbar_wait(&bar_s, t & 1, p.err)) break;
+      tc_fence_after();
+      float pv[64];
+      // query tiles after the diagonal that end inside the sequence need no mask
+      const bool full = t > 0 && q0 + BT <= p.S && k0 + BT <= p.S;
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        uint32_t us[32];
+        tmem_ld32(tmem_addr(tmem, qd, C_S + ch * 64 + c * 32), us);
+        const float4* l4 = reinterpret_cast<const float4*>(lse_s + ch * 64 + c * 32);
+        if (full) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float4 l = l4[k];
+            pv[c * 32 + 4 * k] = ex2(fmaf(__uint_as_float(us[4 * k]), p.sl2, -l.x));
+            pv[c * 32 + 4 * k + 1] = ex2(fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -l.y));
+            pv[c * 32 + 4 * k + 2] = ex2(fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -l.z));
+            pv[c * 32 + 4 * k + 3] = ex2(fmaf(__uint_as_float(us[4 * k + 3]), p.sl2, -l.w));
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 32; ++k) {
+            const int col = ch * 64 + c * 32 + k;
+            const bool ok = key_ok && col >= qlo && col < qhi;
+            pv[c * 32 + k] =
+                ok ? ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[col])) : 0.f;
+          }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(pv[c * 32 + 2 * k], pv[c * 32 + 2 * k + 1]);
+        tmem_st16(tmem_addr(tmem, qd, C_S + ch * 64 + c * 16), pk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p);
+      // ---- phase B: dS^T = P^T (dP^T - delta) * scale, packed into the ends
+      //      of the dP^T columns.  Half 0 reads [384,416) then [416,448) and
+      //      writes [384,400) then [400,416); half 1 reads [480,512) then
+      //      [448,480) and writes [496,512) then [480,496): each write lands
+      //      on columns its own warp has already read.
+      if (!mbar_wait(&bar_dp, t & 1, p.err)) break;
+      tc_fence_after();
+      {
+        const float* dl = dlt_s + ch * 64;
+        const uint32_t rd = tmem_addr(tmem, qd, C_DP + ch * 64);
+        const uint32_t wr = tmem_addr(tmem, qd, C_DP + ch * 96);
+        if (ch == 0) {
+          ds_chunk<0>(rd, wr, pv, dl, p.scale);
+          ds_chunk<1>(rd, wr, pv, dl, p.scale);
+        } else {
+          ds_chunk<1>(rd, wr, pv, dl, p.scale);
+          ds_chunk<0>(rd, wr, pv, dl, p.scale);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_ds);
+      // ---- the k_pe part of dK for this query tile, out of [416,480)
+      if (!mbar_wait(&bar_dkr, t & 1, p.err)) break;
+      tc_fence_after();
+      {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tmem, qd, C_DKR + ch * 32), u);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) acc[k] += __uint_as_float(u[k]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_tfree);
+    }
+    // ---- epilogue: dK_nope (half 0) or dV (half 1) rows, k_pe part of dK
+    if (mbar_wait(&bar_fin, 0, p.err)) {
+      tc_fence_after();
+      __nv_bfloat16* dst = p.dkv + b * p.kv_sb + (long long)key * p.kv_ss + h * p.kv_sh + ch * 128;
+      const int src = ch == 0 ? C_DK : C_DV;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tmem, qd, src + c * 32), u);
+        if (key_ok) {
+          uint4 v4[4];
+          uint32_t* w = reinterpret_cast<uint32_t*>(v4);
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            w[k] = pack_bf16(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1]));
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) d4[k] = v4[k];
+        }
+      }
+      if (key_ok) {
+        float4* d4 = reinterpret_cast<float4*>(p.dkpe + (((long long)b * p.S + key) * p.H + h) * DR +
+                                               ch * 32);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          d4[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attn_bwd_kv(const Plan& p, const Ptrs& x, cudaStream_t st) {
+  Views v = make_views(p, x);
+  const uint64_t S = p.S, H = p.H, B = p.B;
+  KvMaps tm;
+  cudaError_t e;
+  {
+    const uint64_t ld = (uint64_t)v.qn_ld * 2;
+    uint64_t dims[4] = {128, H, S, B}, str[3] = {ld, H * ld, S * H * ld};
+    uint32_t box[4] = {64, 1, 128, 1};
+    if ((e = make_tmap_bf16(&tm.qn, v.qn, 4, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[4] = {64, H, S, B}, str[3] = {128, H * 128, S * H * 128};
+    uint32_t box[4] = {64, 1, 128, 1};
+    if ((e = make_tmap_bf16(&tm.qr, v.qr, 4, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[4] = {128, H, S, B}, str[3] = {256, H * 256, S * H * 256};
+    uint32_t box[4] = {64, 1, 128, 1};
+    if ((e = make_tmap_bf16(&tm.dO, v.dO, 4, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[4] = {256, S, H, B};
+    uint64_t str[3] = {(uint64_t)v.kv_ss * 2, (uint64_t)v.kv_sh * 2, (uint64_t)v.kv_sb * 2};
+    uint32_t box[4] = {64, 128, 1, 1};
+    if ((e = make_tmap_bf16(&tm.kv, v.kv, 4, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[3] = {64, S, B}, str[2] = {128, S * 128};
+    uint32_t box[3] = {64, 128, 1};
+    if ((e = make_tmap_bf16(&tm.kpe, v.kpe, 3, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    // rows padded to a multiple of 128 floats; extent S so TMA zero-fills the tail
+    uint64_t dims[2] = {S, B * H}, str[1] = {(uint64_t)p.s_pad() * 4};
+    uint32_t box[2] = {128, 1};
+    if ((e = make_tmap_f32(&tm.lse, x.buf<float>(p, T_LSE2), 2, dims, str, box)) != cudaSuccess)
+      return e;
+    if ((e = make_tmap_f32(&tm.dlt, x.buf<float>(p, T_DELTA), 2, dims, str, box)) != cudaSuccess)
+      return e;
+  }
+  KvParams prm;
+  prm.S = p.S;
+  prm.H = p.H;
+  prm.B = p.B;
+  prm.n_t = (p.S + BT - 1) / BT;
+  prm.sl2 = p.scale * 1.4426950408889634f;
+  prm.scale = p.scale;
+  prm.dkv = x.buf<__nv_bfloat16>(p, T_DKV);
+  prm.kv_sb = v.kv_sb;
+  prm.kv_ss = v.kv_ss;
+  prm.kv_sh = v.kv_sh;
+  prm.dkpe = x.buf<float>(p, T_DKPE);
+  prm.err = x.err;
+  e = cudaFuncSetAttribute(attn_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)prm.n_t * p.H * p.B;
+  LaunchScope ls_("attn_bwd_dkdv", st);
+  attn_bwd_kv_kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(tm, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace laga

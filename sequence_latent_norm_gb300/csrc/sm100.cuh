@@ -250,6 +250,18 @@ LAGA_DEVINL void named_bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Per-warp register budget changes (setmaxnreg).  The growing warps draw on
+// what the shrinking ones release from the block's launch allocation, so a
+// split must not exceed threads x registers-at-launch.
+template <uint32_t N>
+LAGA_DEVINL void reg_grow() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+LAGA_DEVINL void reg_shrink() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 LAGA_DEVINL int ld_acquire_gpu(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
