@@ -20,7 +20,7 @@
 //              S^T_{i+1} (so the next tile's scores overlap phase B), dK.
 //   warps 10-11 idle (they complete warpgroup 2 for the register split).
 // TMEM columns: dV [0,128), dK_nope [128,256), S^T [256,384) with P^T in
-// [256,288) and [320,352), dP^T [384,512) with dS^T in [384,416) and
+// [256,288) and [352,384), dP^T [384,512) with dS^T in [384,416) and
 // [480,512); the k_pe part of dK for tile i goes to [416,480), the dP^T
 // columns phase B has read and left free.  Every mbarrier is waited phase
 // by phase, so parity waits are exact.
@@ -62,31 +62,14 @@ struct KvParams {
   int* err;
 };
 
-// TMEM column of the K-step s (16 query columns) of the packed P^T tile:
-// query columns 0-63 are packed into [C_S, C_S+32), 64-127 into
-// [C_S+64, C_S+96).
-LAGA_DEVINL uint32_t pt_col(int s) { return s < 4 ? C_S + 8 * s : C_S + 64 + 8 * (s - 4); }
-// The same for the packed dS^T tile, at the two ends of the dP^T columns,
-// [C_DP, C_DP+32) and [C_DP+96, C_DP+128), which leaves [C_DP+32, C_DP+96)
-// for the k_pe part of dK.
-LAGA_DEVINL uint32_t dst_col(int s) { return s < 4 ? C_DP + 8 * s : C_DP + 96 + 8 * (s - 4); }
-
-// Phase B on the 32 query columns [32C, 32C+32) of this warp's half: read
-// dP^T from `rd` + 32C, write dS^T = P^T (dP^T - delta) * scale as 16 packed
-// bf16 pairs to `wr` + 16C.
-template <int C>
-LAGA_DEVINL void ds_chunk(uint32_t rd, uint32_t wr, const float (&pv)[64], const float* dlt,
-                          float scale) {
-  uint32_t ud[32], dk[16];
-  tmem_ld32(rd + C * 32, ud);
-#pragma unroll
-  for (int k = 0; k < 16; ++k) {
-    const float2 dl = reinterpret_cast<const float2*>(dlt + C * 32)[k];
-    const float d0 = pv[C * 32 + 2 * k] * (__uint_as_float(ud[2 * k]) - dl.x) * scale;
-    const float d1 = pv[C * 32 + 2 * k + 1] * (__uint_as_float(ud[2 * k + 1]) - dl.y) * scale;
-    dk[k] = pack_bf16(d0, d1);
-  }
-  tmem_st16(wr + C * 16, dk);
+// Both packed tiles use the same layout: the 16 bf16 pairs of query
+// columns [32c, 32c+32) of half h land at base + 96h + 16c, so half 0 fills
+// [base, base+32) and half 1 [base+96, base+128).  Half 0 walks its chunks
+// c = 0, 1 and half 1 walks c = 1, 0; each write then lands on columns its
+// own warp has already read, and [base+32, base+96) is left free.
+// TMEM column of the K-step s (16 query columns) of a packed tile:
+LAGA_DEVINL uint32_t packed_col(int base, int s) {
+  return s < 4 ? base + 8 * s : base + 96 + 8 * (s - 4);
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -211,7 +194,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DV, tmem + pt_col(s), sdesc_sw128(gb + s * 2048, BOX, 1024), idMN,
+          mma_ts(tmem + C_DV, tmem + packed_col(C_S, s), sdesc_sw128(gb + s * 2048, BOX, 1024), idMN,
                  (t > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_do_free);
         // S^T_{i+1} overwrites P^T_i only after the dV MMAs above read it
@@ -221,12 +204,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DKR, tmem + dst_col(s), sdesc_sw128(qb + 2 * BOX + s * 2048, BOX, 1024),
+          mma_ts(tmem + C_DKR, tmem + packed_col(C_DP, s), sdesc_sw128(qb + 2 * BOX + s * 2048, BOX, 1024),
                  idDKr, s > 0);
         mma_commit(&bar_dkr);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DK, tmem + dst_col(s), sdesc_sw128(qb + s * 2048, BOX, 1024), idMN,
+          mma_ts(tmem + C_DK, tmem + packed_col(C_DP, s), sdesc_sw128(qb + s * 2048, BOX, 1024), idMN,
                  (t > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_q_free[t & 1]);
       }
@@ -258,55 +241,60 @@ __global__ void __launch_bounds__(THREADS, 1)
       // query tiles after the diagonal that end inside the sequence need no mask
       const bool full = t > 0 && q0 + BT <= p.S && k0 + BT <= p.S;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int kk = 0; kk < 2; ++kk) {
+        const int c = kk ^ ch;          // chunk of this pass (see packed_col)
+        const int col0 = ch * 64 + c * 32;
         uint32_t us[32];
-        tmem_ld32(tmem_addr(tmem, qd, C_S + ch * 64 + c * 32), us);
-        const float4* l4 = reinterpret_cast<const float4*>(lse_s + ch * 64 + c * 32);
+        tmem_ld32(tmem_addr(tmem, qd, C_S + col0), us);
+        const float4* l4 = reinterpret_cast<const float4*>(lse_s + col0);
         if (full) {
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const float4 l = l4[k];
-            pv[c * 32 + 4 * k] = ex2(fmaf(__uint_as_float(us[4 * k]), p.sl2, -l.x));
-            pv[c * 32 + 4 * k + 1] = ex2(fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -l.y));
-            pv[c * 32 + 4 * k + 2] = ex2(fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -l.z));
-            pv[c * 32 + 4 * k + 3] = ex2(fmaf(__uint_as_float(us[4 * k + 3]), p.sl2, -l.w));
+            pv[kk * 32 + 4 * k] = ex2(fmaf(__uint_as_float(us[4 * k]), p.sl2, -l.x));
+            pv[kk * 32 + 4 * k + 1] = ex2(fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -l.y));
+            pv[kk * 32 + 4 * k + 2] = ex2(fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -l.z));
+            pv[kk * 32 + 4 * k + 3] = ex2(fmaf(__uint_as_float(us[4 * k + 3]), p.sl2, -l.w));
           }
         } else {
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const int col = ch * 64 + c * 32 + k;
+            const int col = col0 + k;
             const bool ok = key_ok && col >= qlo && col < qhi;
-            pv[c * 32 + k] =
+            pv[kk * 32 + k] =
                 ok ? ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[col])) : 0.f;
           }
         }
         uint32_t pk[16];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(pv[c * 32 + 2 * k], pv[c * 32 + 2 * k + 1]);
-        tmem_st16(tmem_addr(tmem, qd, C_S + ch * 64 + c * 16), pk);
+        for (int k = 0; k < 16; ++k)
+          pk[k] = pack_bf16(pv[kk * 32 + 2 * k], pv[kk * 32 + 2 * k + 1]);
+        tmem_st16(tmem_addr(tmem, qd, C_S + ch * 96 + c * 16), pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p);
-      // ---- phase B: dS^T = P^T (dP^T - delta) * scale, packed into the ends
-      //      of the dP^T columns.  Half 0 reads [384,416) then [416,448) and
-      //      writes [384,400) then [400,416); half 1 reads [480,512) then
-      //      [448,480) and writes [496,512) then [480,496): each write lands
-      //      on columns its own warp has already read.
+      // ---- phase B: dS^T = P^T (dP^T - delta) * scale, packed like P^T
+      //      into the ends of the dP^T columns
       if (!mbar_wait(&bar_dp, t & 1, p.err)) break;
       tc_fence_after();
-      {
-        const float* dl = dlt_s + ch * 64;
-        const uint32_t rd = tmem_addr(tmem, qd, C_DP + ch * 64);
-        const uint32_t wr = tmem_addr(tmem, qd, C_DP + ch * 96);
-        if (ch == 0) {
-          ds_chunk<0>(rd, wr, pv, dl, p.scale);
-          ds_chunk<1>(rd, wr, pv, dl, p.scale);
-        } else {
-          ds_chunk<1>(rd, wr, pv, dl, p.scale);
-          ds_chunk<0>(rd, wr, pv, dl, p.scale);
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int c = kk ^ ch;
+        const int col0 = ch * 64 + c * 32;
+        uint32_t ud[32], dk[16];
+        tmem_ld32(tmem_addr(tmem, qd, C_DP + col0), ud);
+        const float2* d2 = reinterpret_cast<const float2*>(dlt_s + col0);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float2 dl = d2[k];
+          const float d0 = pv[kk * 32 + 2 * k] * (__uint_as_float(ud[2 * k]) - dl.x) * p.scale;
+          const float d1 =
+              pv[kk * 32 + 2 * k + 1] * (__uint_as_float(ud[2 * k + 1]) - dl.y) * p.scale;
+          dk[k] = pack_bf16(d0, d1);
         }
+        tmem_st16(tmem_addr(tmem, qd, C_DP + ch * 96 + c * 16), dk);
       }
       tmem_wait_st();
       tc_fence_before();
