@@ -16,8 +16,9 @@
 //              k_pe part of dK from TMEM into registers.
 //   warp 8     TMA producer: K_j, V_j once; per i: Q_i with LSE_i and
 //              delta_i (double-buffered), dO_i.
-//   warp 9     TMEM allocator and MMA issuer.  Per i: dP^T_i, dV, then
-//              S^T_{i+1} (so the next tile's scores overlap phase B), dK.
+//   warp 9     TMEM allocator and MMA issuer.  Per i: dP^T_i, dV, the
+//              k_nope steps of S^T_{i+1} (overlapping phase B), the k_pe
+//              part of dK, the k_pe steps of S^T_{i+1}, dK_nope.
 //   warps 10-11 idle (they complete warpgroup 2 for the register split).
 // TMEM columns: dV [0,128), dK_nope [128,256), S^T [256,384) with P^T in
 // [256,288) and [352,384), dP^T [384,512) with dS^T in [384,416) and
@@ -159,23 +160,35 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idDKr = idesc_bf16(128, 64, 0, 1);
       const uint32_t kb = smem_u32(sm + K_OFF), vb = smem_u32(sm + V_OFF);
       const uint32_t gb = smem_u32(sm + DO_OFF);
-      // S^T_i = K Q_i^T (12 K-steps over d = 192) into [256,384)
-      auto issue_s = [&](int t) -> bool {
+      // S^T_i = K Q_i^T (12 K-steps over d = 192) into [256,384), in two
+      // parts: the 8 k_nope steps, then the 4 k_pe steps and the commit
+      auto issue_s_nope = [&](int t) -> bool {
         if (!mbar_wait(&bar_q_full[t & 1], (t >> 1) & 1, p.err)) return false;
         tc_fence_after();
         const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
 #pragma unroll
-        for (int s = 0; s < 12; ++s) {
+        for (int s = 0; s < 8; ++s) {
           const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
           mma_ss(tmem + C_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
                  idST, s > 0);
         }
-        mma_commit(&bar_s);
         return true;
       };
-      bool ok = mbar_wait(&bar_kv, 0, p.err) && issue_s(0);
+      auto issue_s_rope = [&](int t) {
+        const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          const uint32_t off = 2 * BOX + s * 32;
+          mma_ss(tmem + C_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
+                 idST, 1u);
+        }
+        mma_commit(&bar_s);
+      };
+      bool ok = mbar_wait(&bar_kv, 0, p.err) && issue_s_nope(0);
+      if (ok) issue_s_rope(0);
       for (int t = 0; ok && t < n_i; ++t) {
         const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
+        const bool next = t + 1 < n_i;
         // dP^T = V dO^T (8 K-steps over d_v) into [384,512): dS^T of tile
         // i-1 there was read by the dK MMAs issued before, and the k_pe part
         // of dK of tile i-1 has been read out once tfree completes
@@ -194,23 +207,27 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DV, tmem + packed_col(C_S, s), sdesc_sw128(gb + s * 2048, BOX, 1024), idMN,
-                 (t > 0 || s > 0) ? 1u : 0u);
+          mma_ts(tmem + C_DV, tmem + packed_col(C_S, s), sdesc_sw128(gb + s * 2048, BOX, 1024),
+                 idMN, (t > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_do_free);
-        // S^T_{i+1} overwrites P^T_i only after the dV MMAs above read it
-        if (t + 1 < n_i && !issue_s(t + 1)) break;
-        // dK_rope_i = dS^T Q_rope into [416,480), dK_nope += dS^T Q_nope
+        // S^T_{i+1} overwrites P^T_i only after the dV MMAs above read it.
+        // Its k_nope steps keep the pipe busy until dS^T_i is ready; the
+        // k_pe part of dK for tile i goes ahead of its k_pe steps, so the
+        // compute warps can read it out while the rest of the pipe runs.
+        if (next && !issue_s_nope(t + 1)) break;
         if (!mbar_wait(&bar_ds, t & 1, p.err)) break;
         tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DKR, tmem + packed_col(C_DP, s), sdesc_sw128(qb + 2 * BOX + s * 2048, BOX, 1024),
-                 idDKr, s > 0);
+          mma_ts(tmem + C_DKR, tmem + packed_col(C_DP, s),
+                 sdesc_sw128(qb + 2 * BOX + s * 2048, BOX, 1024), idDKr, s > 0);
         mma_commit(&bar_dkr);
+        if (next) issue_s_rope(t + 1);
+        // dK_nope += dS^T Q_nope
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DK, tmem + packed_col(C_DP, s), sdesc_sw128(qb + s * 2048, BOX, 1024), idMN,
-                 (t > 0 || s > 0) ? 1u : 0u);
+          mma_ts(tmem + C_DK, tmem + packed_col(C_DP, s), sdesc_sw128(qb + s * 2048, BOX, 1024),
+                 idMN, (t > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_q_free[t & 1]);
       }
       mma_commit(&bar_fin);
