@@ -61,11 +61,10 @@ cudaError_t launch_upproj_bwd(const Plan& p, const Ptrs& x, cudaStream_t st);
 cudaError_t launch_absorbed_fwd(const Plan& p, const Ptrs& x, cudaStream_t st);
 cudaError_t launch_absorbed_bwd(const Plan& p, const Ptrs& x, cudaStream_t st);
 
-// attn_fwd.cu / attn_bwd.cu: causal attention forward and backward.
+// attn_fwd.cu: causal attention forward.  attn_bwd_kv.cu / attn_bwd_dq.cu:
+// its backward, split into a key-stationary dK/dV kernel and a
+// query-stationary dQ kernel.
 cudaError_t launch_attn_fwd(const Plan& p, const Ptrs& x, cudaStream_t st);
-cudaError_t launch_attn_bwd(const Plan& p, const Ptrs& x, cudaStream_t st);
-// attn_bwd_kv.cu / attn_bwd_dq.cu: the backward split into a key-stationary
-// dK/dV kernel and a query-stationary dQ kernel.
 cudaError_t launch_attn_bwd_kv(const Plan& p, const Ptrs& x, cudaStream_t st);
 cudaError_t launch_attn_bwd_dq(const Plan& p, const Ptrs& x, cudaStream_t st);
 

@@ -39,7 +39,6 @@ enum BufId {
   T_DQABS,      // fp32 [B*S*H, 512]    gradient of q_absorbed (absorbed)
   T_DLF,        // (unused)
   T_DWP,        // fp32 [splits, 512, H*256] split-K partials of dW
-  T_SEM,        // int  [B*H*ceil(S/128) + 1] ordered-dQ semaphores + work counter
   N_BUF
 };
 
@@ -65,8 +64,7 @@ static const char* const kBufName[N_BUF] = {
     "L", "ln_mean", "ln_rstd", "k_pe_rot", "q_rope_rot", "kv", "q_absorbed", "o_latent",
     "q_nope_padded", "w_kvb_padded", "o_padded",
     "delta", "lse_log2", "dO_padded", "dq_rot", "dkv", "dk_pe_heads", "dL", "dgamma_partials",
-    "dw_padded", "dO_latent", "dq_absorbed", "dL_attention", "dw_split_partials",
-    "dq_semaphores"};
+    "dw_padded", "dO_latent", "dq_absorbed", "dL_attention", "dw_split_partials"};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -131,7 +129,6 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
     p->len[T_DOLAT] = R * 512 * 2;
     p->len[T_DQABS] = R * 512 * 4;
   }
-  p->len[T_SEM] = ((size_t)p->B * p->H * ((p->S + 127) / 128) + 1) * 4;
   if (!absorbed && dw_splits(p->H) > 1) p->len[T_DWP] = (size_t)dw_splits(p->H) * 512 * H * 256 * 4;
   size_t o = 0;
   for (int i = 0; i < N_SAVED; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }

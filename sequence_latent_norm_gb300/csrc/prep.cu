@@ -125,12 +125,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const T* __restrict__ o,
                                                       const T* __restrict__ d_o, int B, int S,
                                                       int H, int dv, float* __restrict__ delta,
                                                       __nv_bfloat16* __restrict__ do_pad,
-                                                      int* __restrict__ sem, int n_sem,
                                                       const float* __restrict__ lse,
                                                       float* __restrict__ lse2, int s_pad) {
   const int lane = threadIdx.x & 31;
-  // the attention backward's semaphores and work counter start at zero
-  for (int i = blockIdx.x * 256 + threadIdx.x; i < n_sem; i += gridDim.x * 256) sem[i] = 0;
   const long long row = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5);
   if (row >= (long long)B * S * H) return;
   const T* orow = o + row * dv;
@@ -363,9 +360,8 @@ __global__ void __launch_bounds__(256) prep_fwd_v_kernel(
 // delta = rowsum(dO * O): a half-warp per (token, head) row of 128.
 __global__ void __launch_bounds__(256) bwd_pre_v_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ d_o, int S, int H,
-    long long rows, float* __restrict__ delta, int* __restrict__ sem, int n_sem,
+    long long rows, float* __restrict__ delta,
     const float* __restrict__ lse, float* __restrict__ lse2, int s_pad) {
-  for (int i = blockIdx.x * 256 + threadIdx.x; i < n_sem; i += gridDim.x * 256) sem[i] = 0;
   const int sub = threadIdx.x & 15;
   const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
   const bool ok = row < rows;
@@ -583,21 +579,19 @@ cudaError_t launch_bwd_pre(const Plan& p, const Ptrs& x, cudaStream_t st) {
   const int g = grid_for(p.rows(), WARPS);
   float* delta = x.buf<float>(p, T_DELTA);
   __nv_bfloat16* dop = p.canonical ? nullptr : x.buf<__nv_bfloat16>(p, T_DOC);
-  int* sem = x.buf<int>(p, T_SEM);
   float* lse2 = x.buf<float>(p, T_LSE2);
-  const int n_sem = (int)(p.len[T_SEM] / 4);
   if (p.canonical)
     bwd_pre_v_kernel<<<grid_for(p.rows(), 16), 256, 0, st>>>(
-        (const __nv_bfloat16*)x.o, (const __nv_bfloat16*)x.d_o, p.S, p.H, p.rows(), delta, sem,
-        n_sem, x.lse, lse2, (int)p.s_pad());
+        (const __nv_bfloat16*)x.o, (const __nv_bfloat16*)x.d_o, p.S, p.H, p.rows(), delta,
+        x.lse, lse2, (int)p.s_pad());
   else if (p.fp32)
     bwd_pre_kernel<float><<<g, 256, 0, st>>>((const float*)x.o, (const float*)x.d_o, p.B, p.S, p.H,
-                                             p.dv, delta, dop, sem, n_sem, x.lse, lse2,
+                                             p.dv, delta, dop, x.lse, lse2,
                                              (int)p.s_pad());
   else
     bwd_pre_kernel<__nv_bfloat16><<<g, 256, 0, st>>>((const __nv_bfloat16*)x.o,
                                                      (const __nv_bfloat16*)x.d_o, p.B, p.S, p.H,
-                                                     p.dv, delta, dop, sem, n_sem, x.lse, lse2,
+                                                     p.dv, delta, dop, x.lse, lse2,
                                              (int)p.s_pad());
   return cudaGetLastError();
 }

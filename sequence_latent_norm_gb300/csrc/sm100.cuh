@@ -37,9 +37,6 @@ LAGA_DEVINL void mbar_init(uint64_t* bar, uint32_t count) {
 LAGA_DEVINL void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-LAGA_DEVINL void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 LAGA_DEVINL void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -114,33 +111,6 @@ LAGA_DEVINL void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int x, 
       " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z), "r"(w)
       : "memory");
-}
-
-// TMA tensor store / reduce-add from shared memory (bulk-group completion).
-LAGA_DEVINL void tma_store_4d(const void* tmap, const void* src, int x, int y, int z, int w) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(tmap)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
-LAGA_DEVINL void tma_reduce_add_4d(const void* tmap, const void* src, int x, int y, int z, int w) {
-  asm volatile(
-      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.bulk_group [%0, {%2, %3, %4, %5}], "
-      "[%1];" ::"l"(reinterpret_cast<uint64_t>(tmap)),
-      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
-      : "memory");
-}
-LAGA_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until the committed bulk groups have finished reading shared memory.
-LAGA_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Wait until all but the most recent committed bulk group have finished
-// reading shared memory.
-LAGA_DEVINL void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
-// Wait until the committed bulk groups have completed (writes performed).
-LAGA_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-LAGA_DEVINL void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -237,17 +207,11 @@ LAGA_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
       "r"(r[15])
       : "memory");
 }
-LAGA_DEVINL void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 LAGA_DEVINL void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // TMEM address of (lane quadrant of this warp, column).
 LAGA_DEVINL uint32_t tmem_addr(uint32_t base, int warp_in_group, int col) {
   return base + ((uint32_t)(warp_in_group * 32) << 16) + (uint32_t)col;
-}
-
-// Named barrier among `count` threads (ids 1..15; 0 is __syncthreads).
-LAGA_DEVINL void named_bar_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Per-warp register budget changes (setmaxnreg).  The growing warps draw on
@@ -260,15 +224,6 @@ LAGA_DEVINL void reg_grow() {
 template <uint32_t N>
 LAGA_DEVINL void reg_shrink() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
-LAGA_DEVINL int ld_acquire_gpu(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-LAGA_DEVINL void st_release_gpu(int* p, int v) {
-  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 LAGA_DEVINL uint32_t pack_bf16(float lo, float hi) {
