@@ -223,8 +223,8 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
     if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
   } else {
     if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
-    if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, st);
-    if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
+    if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, st);   // canonical: writes dq itself
+    if (e == cudaSuccess && !p.canonical) e = launch_dq_finalize(p, x, st);
     if (e == cudaSuccess) e = launch_upproj_bwd(p, x, st);
   }
   if (e == cudaSuccess && !p.canonical) e = launch_unpad_dw(p, x, st);

@@ -24,6 +24,9 @@
 // TMEM columns: S [0,128), dP [128,256) with dS in [128,160) and [192,224),
 // dQ [256,448), q_nope [448,512).  Every mbarrier is waited phase by phase,
 // so parity waits are exact.
+// Epilogue: for the canonical bf16 layout the kernel writes the final dq,
+// rotating the k_pe band back by the row's position; otherwise it writes
+// fp32 rotated-frame rows that dq_final converts.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -60,7 +63,10 @@ struct DqParams {
   float scale;
   const float* lse2;         // [B*H, s_pad]  LSE * log2(e)
   const float* delta;        // [B*H, s_pad]
-  float* dq;                 // [B, S, H, 192] fp32, rotated frame
+  float* dq;                 // [B, S, H, 192] fp32, rotated frame (when dq_out is null)
+  __nv_bfloat16* dq_out;     // [B, S, H, 192] bf16 final dq, or null
+  const float* cosT;         // [S, 32]
+  const float* sinT;         // [S, 32]
   int* err;
 };
 
@@ -284,17 +290,70 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---- epilogue: this thread's query row, half of its 192 dQ columns
     if (ok && mbar_wait(&bar_fin, 0, p.err)) {
       tc_fence_after();
-      float* dst = p.dq + (((long long)b * p.S + query) * p.H + h) * 192 + ch * 96;
-#pragma unroll 1
-      for (int c = 0; c < 3; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, qd, C_DQ + ch * 96 + c * 32), u);
-        if (q_ok) {
-          float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+      const long long row = ((long long)b * p.S + query) * p.H + h;
+      if (p.dq_out) {
+        // Final bf16 dq.  The k_pe band [128,192) lies wholly in half 1; it
+        // is rotated back by the row's position (the adjoint of the forward
+        // rotate-half RoPE): a' = a cos + b sin, b' = b cos - a sin for the
+        // pairs (128+k, 160+k).
+        __nv_bfloat16* dst = p.dq_out + row * 192 + ch * 96;
+        auto store32 = [&](__nv_bfloat16* d, const float* v) {
+          uint4 w4[4];
+          uint32_t* w = reinterpret_cast<uint32_t*>(w4);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            d4[k] = make_float4(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
-                                __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
+          for (int k = 0; k < 16; ++k) w[k] = pack_bf16(v[2 * k], v[2 * k + 1]);
+          uint4* d4 = reinterpret_cast<uint4*>(d);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) d4[k] = w4[k];
+        };
+        {
+          uint32_t u[32];
+          tmem_ld32(tmem_addr(tmem, qd, C_DQ + ch * 96), u);
+          if (q_ok) store32(dst, reinterpret_cast<const float*>(u));
+        }
+        if (ch == 0) {
+#pragma unroll 1
+          for (int c = 1; c < 3; ++c) {
+            uint32_t u[32];
+            tmem_ld32(tmem_addr(tmem, qd, C_DQ + c * 32), u);
+            if (q_ok) store32(dst + c * 32, reinterpret_cast<const float*>(u));
+          }
+        } else {
+          uint32_t ua[32], ub[32];
+          tmem_ld32(tmem_addr(tmem, qd, C_DQ + 128), ua);
+          tmem_ld32(tmem_addr(tmem, qd, C_DQ + 160), ub);
+          if (q_ok) {
+            const float4* c4 = reinterpret_cast<const float4*>(p.cosT + (long long)query * 32);
+            const float4* s4 = reinterpret_cast<const float4*>(p.sinT + (long long)query * 32);
+            float ra[32], rb[32];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const float4 cv = c4[k], sv = s4[k];
+              const float cs[4] = {cv.x, cv.y, cv.z, cv.w}, sn[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float av = __uint_as_float(ua[4 * k + e]), bv = __uint_as_float(ub[4 * k + e]);
+                ra[4 * k + e] = av * cs[e] + bv * sn[e];
+                rb[4 * k + e] = bv * cs[e] - av * sn[e];
+              }
+            }
+            store32(dst + 32, ra);
+            store32(dst + 64, rb);
+          }
+        }
+      } else {
+        float* dst = p.dq + row * 192 + ch * 96;
+#pragma unroll 1
+        for (int c = 0; c < 3; ++c) {
+          uint32_t u[32];
+          tmem_ld32(tmem_addr(tmem, qd, C_DQ + ch * 96 + c * 32), u);
+          if (q_ok) {
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              d4[k] = make_float4(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
+                                  __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
+          }
         }
       }
     }
@@ -347,7 +406,12 @@ cudaError_t launch_attn_bwd_dq(const Plan& p, const Ptrs& x, cudaStream_t st) {
   prm.scale = p.scale;
   prm.lse2 = x.buf<float>(p, T_LSE2);
   prm.delta = x.buf<float>(p, T_DELTA);
-  prm.dq = x.buf<float>(p, T_DQ);
+  // canonical dims: the kernel writes the final bf16 dq itself; otherwise
+  // fp32 rotated-frame rows for dq_final
+  prm.dq = p.canonical ? nullptr : x.buf<float>(p, T_DQ);
+  prm.dq_out = p.canonical ? static_cast<__nv_bfloat16*>(x.dq) : nullptr;
+  prm.cosT = x.cos;
+  prm.sinT = x.sin;
   prm.err = x.err;
   e = cudaFuncSetAttribute(attn_bwd_dq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            SMEM_BYTES);

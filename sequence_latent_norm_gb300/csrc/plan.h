@@ -119,7 +119,7 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
   p->len[T_DELTA] = (size_t)p->B * H * p->s_pad() * 4;
   p->len[T_LSE2] = (size_t)p->B * H * p->s_pad() * 4;
   if (!p->canonical) p->len[T_DOC] = R * 128 * 2;
-  p->len[T_DQ] = R * 192 * 4;
+  if (absorbed || !p->canonical) p->len[T_DQ] = R * 192 * 4;
   if (!absorbed) p->len[T_DKV] = R * 256 * 2;
   p->len[T_DKPE] = R * 64 * 4;
   p->len[T_DL] = T * 512 * 4;
