@@ -438,6 +438,8 @@ def run_ours(args, rank, world, local_rank):
                        "l2": "flushed between steps by a 512 MB write outside the timed events",
                        "value_definition": "H*S^2*1152 attention FLOPs / full hot-path step time"},
             "pct_of_bf16_peak": round(100 * value / world / peak_tf, 2),
+            # the same work counted over the exact S(S+1)/2 causal pairs
+            "value_exact_causal_pairs": round(value * (S + 1) / S, 3),
             "attn_kernels_tflops": round(attn_flops / (attn_ms * 1e-3) / 1e12, 2),
             "block_tflops": round((attn_flops + up_f) / (ms_per_step * 1e-3) / 1e12, 2),
             "wall_s_timed": round(t_wall, 3),
