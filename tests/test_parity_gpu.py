@@ -26,6 +26,20 @@ def test_small_canonical_dims_match_oracle(case):
     check_grads(got, ref, where=str(case))
 
 
+@pytest.mark.parametrize("case", [
+    dict(S=200, H=2, d_nope=64, d_rope=32, d_v=64, d_kv=256),   # all dims below canonical
+    dict(S=150, H=3, d_kv=256),                                  # canonical heads, narrower latent
+])
+def test_noncanonical_bf16_dims_match_oracle(case):
+    """bf16 I/O with dims other than 128/64/128/512: zero-padded into the
+    canonical layout on device, with dq converted by dq_final."""
+    wl = config(1, **case)
+    got = gpu_run(wl)
+    ref = oracle_run(wl)
+    check_forward(got, ref, str(case))
+    check_grads(got, ref, where=str(case))
+
+
 def test_tiny_fp32_config_sp1_and_sp2():
     wl = config(0)
     cpu = make_inputs(wl)
