@@ -155,7 +155,9 @@ def kernel_work(name: str, S: int, H: int, B: int = 1):
     T, R = B * S, B * S * H
     table = {
         "attn_fwd": ("tensor", pairs * (2 * 192 + 2 * 128)),
-        "attn_bwd": ("tensor", pairs * (6 * 192 + 4 * 128)),
+        # the backward's algorithmic FLOPs, split between its two kernels:
+        # S^T, dP^T, dV and dK in the key-stationary one, dQ in the other
+        # (whose recomputed S and dP are not counted)
         "attn_bwd_dkdv": ("tensor", pairs * (2 * 192 + 2 * 128 + 2 * 128 + 2 * 192)),
         "attn_bwd_dq": ("tensor", pairs * 2 * 192),
         "upproj": ("tensor", 2.0 * T * 512 * H * 256),
