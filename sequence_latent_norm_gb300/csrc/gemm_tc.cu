@@ -4,10 +4,11 @@
 //   UP   KV[t, h, :]  = L[t, :] . W[:, h*256 : h*256+256]        M=tokens N=256/head K=512
 //   DL   dL[t, :]     = sum_h dKV[t, h, :] . W[:, h-cols]^T       M=tokens N=512      K=H*256
 //   DW   dW[:, h-cols] = sum_t L[t, :]^T dKV[t, h, :]             M=512    N=256/head K=tokens
-// One CTA per 128 x 256 output tile; 6 warps: warp 0 TMA producer (4-stage
-// ring), warp 1 TMEM allocator + MMA issuer (M128 N256 K16 steps, fp32
-// accumulator in 256 TMEM columns), warps 2-5 epilogue (TMEM -> registers ->
-// global).  DW splits the token reduction into a fixed number of chunks whose
+// One CTA per 128 x 256 output tile, two CTAs per SM (each one's prologue and
+// epilogue overlap the other's main loop); 6 warps: warp 0 TMA producer
+// (2-stage ring), warp 1 TMEM allocator + MMA issuer (M128 N256 K16 steps,
+// fp32 accumulator in 256 TMEM columns), warps 2-5 epilogue (TMEM ->
+// registers -> global).  DW splits the token reduction into a fixed number of chunks whose
 // fp32 partial tiles are summed afterwards in chunk order, so every run adds
 // in the same order.  Each output element is one accumulation over K in
 // ascending K-step order whatever the K/V layout, which keeps the
