@@ -54,6 +54,7 @@ constexpr uint32_t V_BYTES = 2 * BOX;
 
 struct DqMaps {
   CUtensorMap qr, kv, kpe, dO;
+  CUtensorMap dq;            // final bf16 dq [B, S, H, 192], 64 x 128 boxes (canonical dims)
 };
 struct DqParams {
   int S, H, B, n_t, s_pad;
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
+  bool stored = false;   // this thread staged its part of the final dq tile
   const int per = p.H * p.B;
   const int i = p.n_t - 1 - (int)(blockIdx.x / per);   // largest query tiles first
   const int h = (int)(blockIdx.x % per) % p.H;
@@ -295,52 +297,60 @@ __global__ void __launch_bounds__(THREADS, 1)
         // Final bf16 dq.  The k_pe band [128,192) lies wholly in half 1; it
         // is rotated back by the row's position (the adjoint of the forward
         // rotate-half RoPE): a' = a cos + b sin, b' = b cos - a sin for the
-        // pairs (128+k, 160+k).
-        __nv_bfloat16* dst = p.dq_out + row * 192 + ch * 96;
-        auto store32 = [&](__nv_bfloat16* d, const float* v) {
-          uint4 w4[4];
-          uint32_t* w = reinterpret_cast<uint32_t*>(w4);
+        // pairs (128+k, 160+k).  The tile is staged in the (now idle) K ring
+        // as three 128 x 64 boxes with 128-byte swizzling and written by TMA
+        // after the final barrier; rows past the sequence are clipped there.
+        uint8_t* stage = sm + K_OFF;
+        // 32 columns starting at c0 (a multiple of 32) of this thread's row
+        auto stage32 = [&](int c0, const float* v) {
+          uint8_t* box = stage + (c0 >> 6) * BOX + r * 128;
+          const int k0 = (c0 & 63) >> 3;
 #pragma unroll
-          for (int k = 0; k < 16; ++k) w[k] = pack_bf16(v[2 * k], v[2 * k + 1]);
-          uint4* d4 = reinterpret_cast<uint4*>(d);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) d4[k] = w4[k];
+          for (int g = 0; g < 4; ++g) {
+            uint4 w;
+            w.x = pack_bf16(v[8 * g], v[8 * g + 1]);
+            w.y = pack_bf16(v[8 * g + 2], v[8 * g + 3]);
+            w.z = pack_bf16(v[8 * g + 4], v[8 * g + 5]);
+            w.w = pack_bf16(v[8 * g + 6], v[8 * g + 7]);
+            *reinterpret_cast<uint4*>(box + (((k0 + g) ^ (r & 7)) << 4)) = w;
+          }
         };
         {
           uint32_t u[32];
           tmem_ld32(tmem_addr(tmem, qd, C_DQ + ch * 96), u);
-          if (q_ok) store32(dst, reinterpret_cast<const float*>(u));
+          stage32(ch * 96, reinterpret_cast<const float*>(u));
         }
         if (ch == 0) {
 #pragma unroll 1
           for (int c = 1; c < 3; ++c) {
             uint32_t u[32];
             tmem_ld32(tmem_addr(tmem, qd, C_DQ + c * 32), u);
-            if (q_ok) store32(dst + c * 32, reinterpret_cast<const float*>(u));
+            stage32(c * 32, reinterpret_cast<const float*>(u));
           }
         } else {
           uint32_t ua[32], ub[32];
           tmem_ld32(tmem_addr(tmem, qd, C_DQ + 128), ua);
           tmem_ld32(tmem_addr(tmem, qd, C_DQ + 160), ub);
-          if (q_ok) {
-            const float4* c4 = reinterpret_cast<const float4*>(p.cosT + (long long)query * 32);
-            const float4* s4 = reinterpret_cast<const float4*>(p.sinT + (long long)query * 32);
-            float ra[32], rb[32];
+          float ra[32], rb[32];
+          const long long pos = q_ok ? query : 0;
+          const float4* c4 = reinterpret_cast<const float4*>(p.cosT + pos * 32);
+          const float4* s4 = reinterpret_cast<const float4*>(p.sinT + pos * 32);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const float4 cv = c4[k], sv = s4[k];
-              const float cs[4] = {cv.x, cv.y, cv.z, cv.w}, sn[4] = {sv.x, sv.y, sv.z, sv.w};
+          for (int k = 0; k < 8; ++k) {
+            const float4 cv = c4[k], sv = s4[k];
+            const float cs[4] = {cv.x, cv.y, cv.z, cv.w}, sn[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float av = __uint_as_float(ua[4 * k + e]), bv = __uint_as_float(ub[4 * k + e]);
-                ra[4 * k + e] = av * cs[e] + bv * sn[e];
-                rb[4 * k + e] = bv * cs[e] - av * sn[e];
-              }
+            for (int e = 0; e < 4; ++e) {
+              const float av = __uint_as_float(ua[4 * k + e]), bv = __uint_as_float(ub[4 * k + e]);
+              ra[4 * k + e] = av * cs[e] + bv * sn[e];
+              rb[4 * k + e] = bv * cs[e] - av * sn[e];
             }
-            store32(dst + 32, ra);
-            store32(dst + 64, rb);
           }
+          stage32(128, ra);
+          stage32(160, rb);
         }
+        fence_proxy_async_smem();
+        stored = true;
       } else {
         float* dst = p.dq + row * 192 + ch * 96;
 #pragma unroll 1
@@ -360,6 +370,13 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && stored) {
+    // the staged dq tile: columns [0,64), [64,128), [128,192)
+#pragma unroll
+    for (int bx = 0; bx < 3; ++bx) tma_store_4d(&tm.dq, sm + K_OFF + bx * BOX, bx * 64, h, q0, b);
+    bulk_commit();
+    bulk_wait_read0();
+  }
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -393,6 +410,11 @@ cudaError_t launch_attn_bwd_dq(const Plan& p, const Ptrs& x, cudaStream_t st) {
     uint64_t dims[3] = {64, S, B}, str[2] = {128, S * 128};
     uint32_t box[3] = {64, 128, 1};
     if ((e = make_tmap_bf16(&tm.kpe, v.kpe, 3, dims, str, box)) != cudaSuccess) return e;
+  }
+  if (p.canonical) {
+    uint64_t dims[4] = {192, H, S, B}, str[3] = {192 * 2, H * 192 * 2, S * H * 192 * 2};
+    uint32_t box[4] = {64, 1, 128, 1};
+    if ((e = make_tmap_bf16(&tm.dq, x.dq, 4, dims, str, box)) != cudaSuccess) return e;
   }
   DqParams prm;
   prm.S = p.S;

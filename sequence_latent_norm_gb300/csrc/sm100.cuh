@@ -113,6 +113,23 @@ LAGA_DEVINL void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int x, 
       : "memory");
 }
 
+// TMA tensor store from shared memory (bulk-group completion).  The source
+// tile is written by ordinary stores first, made visible to the async proxy
+// with fence_proxy_async_smem().
+LAGA_DEVINL void tma_store_4d(const void* tmap, const void* src, int x, int y, int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(tmap)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "r"(w)
+      : "memory");
+}
+LAGA_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed bulk groups have finished reading shared memory.
+LAGA_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+LAGA_DEVINL void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ tcgen05
 // Instruction descriptor of kind::f16 with bf16 A/B and an fp32 accumulator.
 // a_mn / b_mn select MN-major (transposed) operands.
