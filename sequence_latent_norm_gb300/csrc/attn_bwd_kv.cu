@@ -52,6 +52,8 @@ constexpr uint32_t DO_BYTES = 2 * BOX;
 
 struct KvMaps {
   CUtensorMap qn, qr, kv, kpe, dO, lse, dlt;
+  CUtensorMap dkv;           // dK_nope | dV rows, 64 x 128 bf16 boxes
+  CUtensorMap dkpe;          // per-head k_pe part of dK, 32 x 128 fp32 boxes
 };
 struct KvParams {
   int S, H, B, n_t;
@@ -108,6 +110,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
+  bool stored = false;   // this thread staged its rows of the dK / dV tile
   const int per = p.H * p.B;
   const int j = (int)(blockIdx.x / per);   // smallest key tiles (longest walks) first
   const int h = (int)(blockIdx.x % per) % p.H;
@@ -330,37 +333,53 @@ __global__ void __launch_bounds__(THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tfree);
     }
-    // ---- epilogue: dK_nope (half 0) or dV (half 1) rows, k_pe part of dK
+    // ---- epilogue: dK_nope (half 0) or dV (half 1) rows as bf16, and the
+    //      k_pe part of dK as fp32, staged in the idle Q buffers as 128-byte
+    //      swizzled boxes (four 64-column bf16 boxes, two 32-column fp32
+    //      boxes) and written by TMA after the final barrier; rows past the
+    //      sequence are clipped there
     if (mbar_wait(&bar_fin, 0, p.err)) {
       tc_fence_after();
-      __nv_bfloat16* dst = p.dkv + b * p.kv_sb + (long long)key * p.kv_ss + h * p.kv_sh + ch * 128;
+      uint8_t* stage = sm + Q_OFF;
       const int src = ch == 0 ? C_DK : C_DV;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t u[32];
         tmem_ld32(tmem_addr(tmem, qd, src + c * 32), u);
-        if (key_ok) {
-          uint4 v4[4];
-          uint32_t* w = reinterpret_cast<uint32_t*>(v4);
+        uint8_t* box = stage + (ch * 2 + (c >> 1)) * BOX + r * 128;
+        const int k0 = (c & 1) * 4;
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            w[k] = pack_bf16(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1]));
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) d4[k] = v4[k];
+        for (int g = 0; g < 4; ++g) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(u[8 * g]), __uint_as_float(u[8 * g + 1]));
+          w.y = pack_bf16(__uint_as_float(u[8 * g + 2]), __uint_as_float(u[8 * g + 3]));
+          w.z = pack_bf16(__uint_as_float(u[8 * g + 4]), __uint_as_float(u[8 * g + 5]));
+          w.w = pack_bf16(__uint_as_float(u[8 * g + 6]), __uint_as_float(u[8 * g + 7]));
+          *reinterpret_cast<uint4*>(box + (((k0 + g) ^ (r & 7)) << 4)) = w;
         }
       }
-      if (key_ok) {
-        float4* d4 = reinterpret_cast<float4*>(p.dkpe + (((long long)b * p.S + key) * p.H + h) * DR +
-                                               ch * 32);
+      {
+        uint8_t* box = stage + (4 + ch) * BOX + r * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          d4[k] = make_float4(acc[4 * k], acc[4 * k + 1], acc[4 * k + 2], acc[4 * k + 3]);
+        for (int g = 0; g < 8; ++g)
+          *reinterpret_cast<float4*>(box + ((g ^ (r & 7)) << 4)) =
+              make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
       }
+      fence_proxy_async_smem();
+      stored = true;
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && stored) {
+#pragma unroll
+    for (int bx = 0; bx < 4; ++bx) tma_store_4d(&tm.dkv, sm + Q_OFF + bx * BOX, bx * 64, k0, h, b);
+#pragma unroll
+    for (int cx = 0; cx < 2; ++cx)
+      tma_store_4d(&tm.dkpe, sm + Q_OFF + (4 + cx) * BOX, cx * 32, h, k0, b);
+    bulk_commit();
+    bulk_wait_read0();
+  }
   if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -408,6 +427,19 @@ cudaError_t launch_attn_bwd_kv(const Plan& p, const Ptrs& x, cudaStream_t st) {
     if ((e = make_tmap_f32(&tm.lse, x.buf<float>(p, T_LSE2), 2, dims, str, box)) != cudaSuccess)
       return e;
     if ((e = make_tmap_f32(&tm.dlt, x.buf<float>(p, T_DELTA), 2, dims, str, box)) != cudaSuccess)
+      return e;
+  }
+  {
+    uint64_t dims[4] = {256, S, H, B};
+    uint64_t str[3] = {(uint64_t)v.kv_ss * 2, (uint64_t)v.kv_sh * 2, (uint64_t)v.kv_sb * 2};
+    uint32_t box[4] = {64, 128, 1, 1};
+    if ((e = make_tmap_bf16(&tm.dkv, x.buf<__nv_bfloat16>(p, T_DKV), 4, dims, str, box)) != cudaSuccess)
+      return e;
+  }
+  {
+    uint64_t dims[4] = {64, H, S, B}, str[3] = {64 * 4, H * 64 * 4, S * H * 64 * 4};
+    uint32_t box[4] = {32, 1, 128, 1};
+    if ((e = make_tmap_f32(&tm.dkpe, x.buf<float>(p, T_DKPE), 4, dims, str, box, true)) != cudaSuccess)
       return e;
   }
   KvParams prm;
