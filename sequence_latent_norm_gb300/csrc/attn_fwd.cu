@@ -50,6 +50,7 @@ constexpr float LN2 = 0.6931471805599453f;
 
 struct FwdMaps {
   CUtensorMap qn, qr, kv, kpe;
+  CUtensorMap o;            // O [B, S, H, 128] bf16, 64 x 128 boxes
 };
 struct FwdParams {
   int S, H, B, n_qt;
@@ -109,6 +110,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
+  bool stored = false;   // this thread staged its half row of the O tile
 
   if (warp == W_PROD) {
     // Q, then K_j into its ring stage as soon as S_{j-2} has read it
@@ -274,27 +276,37 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const float lt = l + red_l[ch ^ 1][r];
       const float inv = 1.0f / lt;
-      __nv_bfloat16* orow = p.O + (((long long)b * p.S + qi) * p.H + h) * 128 + ch * 64;
+      // O rows staged in the (now idle) Q tile as two 128 x 64 swizzled
+      // boxes and written by TMA after the final barrier; rows past the
+      // sequence are clipped there
+      uint8_t* box = Qs + ch * BOX + r * 128;
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t u[32];
         tmem_ld32(tmem_addr(tmem, qd, O_COL + ch * 64 + c * 32), u);
-        uint4 v4[4];
-        uint32_t* w = reinterpret_cast<uint32_t*>(v4);
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          w[k] = pack_bf16(__uint_as_float(u[2 * k]) * inv, __uint_as_float(u[2 * k + 1]) * inv);
-        if (qi < p.S) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = v4[k];
+        for (int g = 0; g < 4; ++g) {
+          uint4 w;
+          w.x = pack_bf16(__uint_as_float(u[8 * g]) * inv, __uint_as_float(u[8 * g + 1]) * inv);
+          w.y = pack_bf16(__uint_as_float(u[8 * g + 2]) * inv, __uint_as_float(u[8 * g + 3]) * inv);
+          w.z = pack_bf16(__uint_as_float(u[8 * g + 4]) * inv, __uint_as_float(u[8 * g + 5]) * inv);
+          w.w = pack_bf16(__uint_as_float(u[8 * g + 6]) * inv, __uint_as_float(u[8 * g + 7]) * inv);
+          *reinterpret_cast<uint4*>(box + (((c * 4 + g) ^ (r & 7)) << 4)) = w;
         }
       }
+      fence_proxy_async_smem();
+      stored = true;
       if (ch == 0 && qi < p.S) p.lse[((long long)b * p.H + h) * p.S + qi] = (m + log2f(lt)) * LN2;
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == 0 && stored) {
+    tma_store_4d(&tm.o, Qs, 0, h, q0, b);
+    tma_store_4d(&tm.o, Qs + BOX, 64, h, q0, b);
+    bulk_commit();
+    bulk_wait_read0();
+  }
   if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
@@ -329,6 +341,11 @@ cudaError_t launch_attn_fwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
     uint64_t dims[3] = {64, S, B}, str[2] = {128, S * 128};
     uint32_t box[3] = {64, 128, 1};
     if ((e = make_tmap_bf16(&tm.kpe, v.kpe, 3, dims, str, box)) != cudaSuccess) return e;
+  }
+  {
+    uint64_t dims[4] = {128, H, S, B}, str[3] = {128 * 2, H * 128 * 2, S * H * 128 * 2};
+    uint32_t box[4] = {64, 1, 128, 1};
+    if ((e = make_tmap_bf16(&tm.o, v.O, 4, dims, str, box)) != cudaSuccess) return e;
   }
   FwdParams prm;
   prm.S = p.S;
