@@ -34,6 +34,7 @@ enum Mode { UP = 0, DL = 1, DW = 2 };
 
 struct GemmMaps {
   CUtensorMap a, b;
+  CUtensorMap o;      // UP: KV output, 64 x 128 bf16 boxes
 };
 struct GemmParams {
   int S, H, B;
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(THREADS, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_sh;
+  bool staged = false;   // UP: this epilogue thread staged its row of the tile
 
   if (warp == 0) {
     if (lane == 0) {
@@ -141,6 +143,7 @@ __global__ void __launch_bounds__(THREADS, 2)
     const int r = q * 32 + lane;
     const bool have = k_count > 0;
     if (mbar_wait(&bar_done, 0, p.err)) {
+      staged = true;
       tc_fence_after();
       const int row = m0 + r;
 #pragma unroll 1
@@ -153,16 +156,18 @@ __global__ void __launch_bounds__(THREADS, 2)
           for (int k = 0; k < 32; ++k) u[k] = 0u;
         }
         if (MODE == UP) {
-          if (row < p.S) {
-            __nv_bfloat16* dst = p.kv + zz * p.kv_sb + row * p.kv_ss + n_tile * p.kv_sh + c * 32;
-            uint4 v4[4];
-            uint32_t* w = reinterpret_cast<uint32_t*>(v4);
+          // staged in the idle ring as four 128 x 64 swizzled boxes, written
+          // by TMA after the final barrier (rows past the sequence clipped)
+          uint8_t* box = sm + (c >> 1) * (BM * 128) + r * 128;
+          const int k0 = (c & 1) * 4;
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-              w[k] = pack_bf16(__uint_as_float(u[2 * k]), __uint_as_float(u[2 * k + 1]));
-            uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) d4[k] = v4[k];
+          for (int g = 0; g < 4; ++g) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(u[8 * g]), __uint_as_float(u[8 * g + 1]));
+            w.y = pack_bf16(__uint_as_float(u[8 * g + 2]), __uint_as_float(u[8 * g + 3]));
+            w.z = pack_bf16(__uint_as_float(u[8 * g + 4]), __uint_as_float(u[8 * g + 5]));
+            w.w = pack_bf16(__uint_as_float(u[8 * g + 6]), __uint_as_float(u[8 * g + 7]));
+            *reinterpret_cast<uint4*>(box + (((k0 + g) ^ (r & 7)) << 4)) = w;
           }
         } else {
           float* dst;
@@ -185,8 +190,16 @@ __global__ void __launch_bounds__(THREADS, 2)
       }
     }
   }
+  if (MODE == UP && warp >= 2) fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
+  if (MODE == UP && threadIdx.x == 64 && staged) {
+#pragma unroll
+    for (int bx = 0; bx < BN / 64; ++bx)
+      tma_store_4d(&tm.o, sm + bx * (BM * 128), bx * 64, m0, n_tile, zz);
+    bulk_commit();
+    bulk_wait_read0();
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 256);
@@ -243,6 +256,7 @@ cudaError_t launch_upproj(const Plan& p, const Ptrs& x, cudaStream_t st) {
     uint32_t box[2] = {64, 64};
     if ((e = make_tmap_bf16(&tm.b, v.W, 2, dims, str, box)) != cudaSuccess) return e;
   }
+  if ((e = kv_map(&tm.o, p, v, v.kv, 128)) != cudaSuccess) return e;
   GemmParams prm{};
   prm.S = p.S; prm.H = p.H; prm.B = p.B;
   prm.k_steps = 512 / BK;
