@@ -34,7 +34,7 @@ enum Mode { UP = 0, DL = 1, DW = 2 };
 
 struct GemmMaps {
   CUtensorMap a, b;
-  CUtensorMap o;      // UP: KV output, 64 x 128 bf16 boxes
+  CUtensorMap o;      // output: UP KV, 64 x 128 bf16 boxes; DL / DW fp32, 32 x 32 boxes
 };
 struct GemmParams {
   int S, H, B;
@@ -170,21 +170,27 @@ __global__ void __launch_bounds__(THREADS, 2)
             *reinterpret_cast<uint4*>(box + (((k0 + g) ^ (r & 7)) << 4)) = w;
           }
         } else {
-          float* dst;
-          bool ok;
-          if (MODE == DL) {
-            ok = row < p.S;
-            dst = p.out + ((long long)zz * p.S + row) * p.out_ld + n_tile * BN + c * 32;
-          } else {
-            ok = row < 512;
-            dst = p.out + zz * p.split_stride + (long long)row * p.out_ld + n_tile * BN + c * 32;
-          }
-          if (ok) {
-            float4* d4 = reinterpret_cast<float4*>(dst);
+          // fp32 output: each epilogue warp stages its own 32 rows, four
+          // 32 x 32 swizzled boxes at a time, and lane 0 stores them by TMA
+          // (rows past the output are clipped there); no block barrier
+          uint8_t* wst = sm + q * 16384 + (c & 3) * 4096 + lane * 128;
 #pragma unroll
-            for (int k = 0; k < 8; ++k)
-              d4[k] = make_float4(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
-                                  __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
+          for (int g = 0; g < 8; ++g)
+            *reinterpret_cast<float4*>(wst + ((g ^ (lane & 7)) << 4)) =
+                make_float4(__uint_as_float(u[4 * g]), __uint_as_float(u[4 * g + 1]),
+                            __uint_as_float(u[4 * g + 2]), __uint_as_float(u[4 * g + 3]));
+          if ((c & 3) == 3) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc)
+                tma_store_3d(&tm.o, sm + q * 16384 + cc * 4096, n_tile * BN + (c - 3 + cc) * 32,
+                             m0 + q * 32, zz);
+              bulk_commit();
+              bulk_wait_read0();
+            }
+            __syncwarp();
           }
         }
       }
@@ -289,6 +295,12 @@ cudaError_t launch_upproj_bwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
     prm.out = splits > 1 ? x.buf<float>(p, T_DWP) : dw;
     prm.out_ld = (long long)p.H * 256;
     prm.split_stride = 512LL * p.H * 256;
+    {
+      uint64_t dims[3] = {(uint64_t)prm.out_ld, 512, (uint64_t)splits};
+      uint64_t str[2] = {(uint64_t)prm.out_ld * 4, (uint64_t)prm.split_stride * 4};
+      uint32_t box[3] = {32, 32, 1};
+      if ((e = make_tmap_f32(&tm.o, prm.out, 3, dims, str, box, true)) != cudaSuccess) return e;
+    }
     prm.err = x.err;
     dim3 grid(p.H, 512 / BM, splits);
     if ((e = launch<DW>("upproj_dw", tm, prm, grid, st)) != cudaSuccess) return e;
@@ -314,6 +326,11 @@ cudaError_t launch_upproj_bwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
     prm.k_steps = p.H * 4;
     prm.out = x.buf<float>(p, T_DL);
     prm.out_ld = 512;
+    {
+      uint64_t dims[3] = {512, (uint64_t)p.S, (uint64_t)p.B}, str[2] = {512 * 4, (uint64_t)p.S * 512 * 4};
+      uint32_t box[3] = {32, 32, 1};
+      if ((e = make_tmap_f32(&tm.o, prm.out, 3, dims, str, box, true)) != cudaSuccess) return e;
+    }
     prm.err = x.err;
     dim3 grid(2, (p.S + BM - 1) / BM, p.B);
     return launch<DL>("upproj_dl", tm, prm, grid, st);
