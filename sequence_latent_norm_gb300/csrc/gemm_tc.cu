@@ -8,7 +8,7 @@
 // epilogue overlap the other's main loop); 6 warps: warp 0 TMA producer
 // (2-stage ring), warp 1 TMEM allocator + MMA issuer (M128 N256 K16 steps,
 // fp32 accumulator in 256 TMEM columns), warps 2-5 epilogue (TMEM ->
-// registers -> global).  DW splits the token reduction into a fixed number of chunks whose
+// registers -> swizzled tiles in the idle ring -> TMA tensor stores).  DW splits the token reduction into a fixed number of chunks whose
 // fp32 partial tiles are summed afterwards in chunk order, so every run adds
 // in the same order.  Each output element is one accumulation over K in
 // ascending K-step order whatever the K/V layout, which keeps the
