@@ -21,7 +21,7 @@
 //              K-steps) is issued before O += P_j V_j (8 K-steps, P from
 //              TMEM), so the tensor core works on the next tile while the
 //              softmax warps handle this one.
-// Epilogue: O / l rows are staged as bf16 in the idle Q tile (two 128 x 64
+// Epilogue: the rows of O, divided by l, are staged as bf16 in the idle Q tile (two 128 x 64
 // swizzled boxes) and written by TMA stores after the final barrier.
 // TMEM columns: S/P double buffer [0,256) (P of key columns 0-63 packed into
 // the first 32 columns of a buffer, of 64-127 into columns 64-95), O
