@@ -145,7 +145,6 @@ __global__ void __launch_bounds__(THREADS, 2)
     if (mbar_wait(&bar_done, 0, p.err)) {
       staged = true;
       tc_fence_after();
-      const int row = m0 + r;
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t u[32];
