@@ -29,10 +29,13 @@
  *     [head_offset, head_offset + n_h_shard).
  *
  * Ownership and execution.  The caller allocates every buffer (device
- * memory unless stated otherwise).  The library never allocates, frees or
- * synchronises (except laga_sync_check); every call only validates its
- * arguments on the host and enqueues kernels on `stream` (a cudaStream_t
- * passed as void*, NULL = legacy default stream).  Outputs are overwritten,
+ * memory unless stated otherwise).  The library never allocates device
+ * memory, never frees and never synchronises (except laga_sync_check); every
+ * call only validates its arguments on the host and enqueues kernels on
+ * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream).
+ * The one exception to single-stream execution is laga_bwd (below), which
+ * forks part of its work onto a library-owned side stream and joins it back
+ * into `stream`.  Outputs are overwritten,
  * not accumulated.  Summing the partial dc and dgamma of several head shards
  * is the caller's job (the reduce-scatter / all-reduce of Section 5.2).
  *
@@ -132,7 +135,15 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
  *          shard's columns of W_kv_b (output)
  *   dgamma [d_kv] fp32: this shard's partial (output)
  *   ws_saved: the forward's saved workspace (read only)
- *   ws_bwd / bwd_bytes: LAGA_WS_BWD scratch. */
+ *   ws_bwd / bwd_bytes: LAGA_WS_BWD scratch.
+ * Two of the attention backward's kernels are independent.  For the LAGA
+ * and explicit forms one of them runs on a side stream of the library's
+ * own: one stream and two events per device, created on the first call
+ * and kept for the process.  The side stream forks from `stream` and joins
+ * back into it with events, so all of the call's work is ordered before
+ * anything enqueued on `stream` afterwards.  Concurrent calls on one device
+ * are serialised while they enqueue.  While per-kernel profiling is enabled,
+ * every kernel runs on `stream`. */
 laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
                      const float* gamma, const float* cos, const float* sin,
                      const void* o, const float* lse, const void* d_o,

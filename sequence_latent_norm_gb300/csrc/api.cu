@@ -115,6 +115,32 @@ using namespace laga;
 // One thread waits, with a short bound (2^16 polls, ~17 ms), on an mbarrier
 // that nothing arrives on, then records the timeout code in the device error
 // word -- the same path every kernel's bounded waits take.
+// A second stream per device on which the dQ kernel runs beside the dK/dV
+// kernel (the two are independent), forked from and joined back into the
+// caller's stream with events, so the caller sees plain stream order.
+struct SideStream {
+  cudaStream_t st = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+};
+// Held while one call forks onto, and joins back from, the side stream (the
+// events are shared by all calls on a device).
+static std::mutex g_side_mu;
+static cudaError_t side_stream(SideStream** out) {
+  static SideStream per_dev[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SideStream& s = per_dev[dev];
+  if (!s.st) {
+    if ((e = cudaStreamCreateWithFlags(&s.st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming)) != cudaSuccess) return e;
+  }
+  *out = &s;
+  return cudaSuccess;
+}
+
 static __global__ void selftest_wait_timeout_kernel(int* err) {
   __shared__ uint64_t bar;
   laga::sm100::mbar_init(&bar, 1);
@@ -222,8 +248,23 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
     if (e == cudaSuccess) e = launch_absorbed_bwd(p, x, st);
     if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
   } else {
-    if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
-    if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, st);   // canonical: writes dq itself
+    // dQ and dK/dV are independent: dQ runs on a side stream so that each
+    // kernel's last wave is filled by the other's CTAs.  With per-kernel
+    // profiling on they run in turn, so that each one's events time it alone.
+    if (g_prof_on) {
+      if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, st);   // canonical: writes dq itself
+      if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
+    } else {
+      std::lock_guard<std::mutex> lock(g_side_mu);
+      SideStream* side = nullptr;
+      if (e == cudaSuccess) e = side_stream(&side);
+      if (e == cudaSuccess) e = cudaEventRecord(side->fork, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
+      if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, side->st);
+      if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
+      if (e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
+    }
     if (e == cudaSuccess && !p.canonical) e = launch_dq_finalize(p, x, st);
     if (e == cudaSuccess) e = launch_upproj_bwd(p, x, st);
   }
