@@ -139,7 +139,9 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
  * Two of the attention backward's kernels are independent.  For the LAGA
  * and explicit forms one of them runs on a side stream of the library's
  * own: one stream and two events per device, created on the first call
- * and kept for the process.  The side stream forks from `stream` and joins
+ * and kept for the process (so make the first call on a device outside any
+ * stream capture; later calls can be captured: the fork and join are the
+ * usual event record / wait pair).  The side stream forks from `stream` and joins
  * back into it with events, so all of the call's work is ordered before
  * anything enqueued on `stream` afterwards.  Concurrent calls on one device
  * are serialised while they enqueue.  While per-kernel profiling is enabled,
