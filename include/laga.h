@@ -142,8 +142,8 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
  * and kept for the process (so make the first call on a device outside any
  * stream capture; later calls can be captured: the fork and join are the
  * usual event record / wait pair).  The side stream forks from `stream` and joins
- * back into it with events, so all of the call's work is ordered before
- * anything enqueued on `stream` afterwards.  Concurrent calls on one device
+ * back into it with events at the end of the call, so all of the call's
+ * work is ordered before anything enqueued on `stream` afterwards.  Concurrent calls on one device
  * are serialised while they enqueue.  While per-kernel profiling is enabled,
  * every kernel runs on `stream`. */
 laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,

@@ -243,33 +243,41 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
   x.ws_bwd = static_cast<unsigned char*>(ws_bwd);
   if ((s = err_word(&x.err)) != LAGA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // dQ and dK/dV are independent, and nothing after them reads dq: dK/dV
+  // goes first on the caller's stream, dQ beside it on a side stream, so that
+  // dQ's CTAs fill dK/dV's last wave and the up-projection and norm backward
+  // (which need only dK/dV) fill dQ's.  The side stream joins back at the end
+  // (before dq_finalize where that reads dQ's rows).  With per-kernel
+  // profiling on, everything runs in turn on the caller's stream, so that
+  // each kernel's events time it alone.
+  const bool fork = !absorbed && !g_prof_on;
+  std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
+  SideStream* side = nullptr;
   cudaError_t e = launch_bwd_pre(p, x, st);
   if (absorbed) {
     if (e == cudaSuccess) e = launch_absorbed_bwd(p, x, st);
     if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
   } else {
-    // dQ and dK/dV are independent: dQ runs on a side stream so that each
-    // kernel's last wave is filled by the other's CTAs.  With per-kernel
-    // profiling on they run in turn, so that each one's events time it alone.
-    if (g_prof_on) {
-      if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, st);   // canonical: writes dq itself
-      if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
-    } else {
-      std::lock_guard<std::mutex> lock(g_side_mu);
-      SideStream* side = nullptr;
+    cudaStream_t dq_st = st;
+    if (fork) {
+      lock.lock();
       if (e == cudaSuccess) e = side_stream(&side);
       if (e == cudaSuccess) e = cudaEventRecord(side->fork, st);
       if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
-      if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, side->st);
-      if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
-      if (e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
+      if (e == cudaSuccess) dq_st = side->st;
     }
-    if (e == cudaSuccess && !p.canonical) e = launch_dq_finalize(p, x, st);
+    if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
+    if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, dq_st);   // canonical: writes dq itself
+    if (fork && e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
+    if (!p.canonical) {
+      if (fork && e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
+      if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
+    }
     if (e == cudaSuccess) e = launch_upproj_bwd(p, x, st);
   }
   if (e == cudaSuccess && !p.canonical) e = launch_unpad_dw(p, x, st);
   if (e == cudaSuccess) e = launch_norm_bwd(p, x, x.buf<float>(p, T_DL), st);
+  if (fork && p.canonical && side && e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
   return cuda_status(e);
 }
 
