@@ -380,8 +380,8 @@ cudaError_t launch_upproj_bwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
       if ((e = make_tmap_bf16(&tm.a, v.L, 3, dims, str, box)) != cudaSuccess) return e;
     }
     if ((e = kv_map(&tm.b, p, v, dkv, 64)) != cudaSuccess) return e;
-    const int splits = dw_splits(p.H);
     const int total = p.B * ((p.S + 63) / 64);
+    const int splits = dw_splits(p.H, total);
     GemmParams prm{};
     prm.S = p.S; prm.H = p.H; prm.B = p.B;
     prm.m_rows = 512;

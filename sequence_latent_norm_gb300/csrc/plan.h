@@ -68,11 +68,25 @@ static const char* const kBufName[N_BUF] = {
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Token-reduction splits of the dW GEMM: about 512 CTAs over its 4*H
-// output tiles, at most 8.  Depends on the dims only (fixed summation order).
-inline int dw_splits(int H) {
-  int s = 512 / (4 * H);
-  return s < 1 ? 1 : (s > 8 ? 8 : s);
+// Token-reduction splits of the dW GEMM (at most 8).  Its CTA pairs (76 on
+// 152 SMs) run 2*H*s output tiles of ceil(steps/s) 64-token steps each, and
+// every split past the first writes and re-reads an fp32 partial of the
+// shard's dW (8 MB at 16 heads, costed as ~7 token steps of MMA time).  The
+// count minimising waves x steps + partial traffic depends on the dims only,
+// so the summation order is fixed.
+inline int dw_splits(int H, int token_steps) {
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= 8; ++s) {
+    const long long waves = (2LL * H * s + 75) / 76;
+    const long long steps = (token_steps + s - 1) / s;
+    const long long cost = 16 * waves * steps + (s > 1 ? 7LL * s * H : 0);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
 }
 
 // Validate dims; returns LAGA_OK or the error and fills the plan.
@@ -129,7 +143,8 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
     p->len[T_DOLAT] = R * 512 * 2;
     p->len[T_DQABS] = R * 512 * 4;
   }
-  if (!absorbed && dw_splits(p->H) > 1) p->len[T_DWP] = (size_t)dw_splits(p->H) * 512 * H * 256 * 4;
+  const int splits = dw_splits(p->H, p->B * ((p->S + 63) / 64));
+  if (!absorbed && splits > 1) p->len[T_DWP] = (size_t)splits * 512 * H * 256 * 4;
   size_t o = 0;
   for (int i = 0; i < N_SAVED; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }
   p->saved_bytes = o;
