@@ -357,31 +357,52 @@ __global__ void __launch_bounds__(256) prep_fwd_v_kernel(
   }
 }
 
-// delta = rowsum(dO * O): a half-warp per (token, head) row of 128.
+// delta = rowsum(dO * O): a half-warp per (token, head) row of 128, PRE_ROWS
+// rows per half-warp, all loads issued before any use.  Row k of a block is
+// blockIdx.x * 16 * PRE_ROWS + k * 16 + (half-warp), so each load instruction
+// of the block covers 16 consecutive rows.
+constexpr int PRE_ROWS = 4;
 __global__ void __launch_bounds__(256) bwd_pre_v_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ d_o, int S, int H,
     long long rows, float* __restrict__ delta,
     const float* __restrict__ lse, float* __restrict__ lse2, int s_pad) {
   const int sub = threadIdx.x & 15;
-  const long long row = (long long)blockIdx.x * 16 + (threadIdx.x >> 4);
-  const bool ok = row < rows;
-  float acc = 0.f;
-  if (ok) {
-    float a[8], g[8];
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(o + row * 128 + 8 * sub), a);
-    bf16x8_to_f32(*reinterpret_cast<const uint4*>(d_o + row * 128 + 8 * sub), g);
+  const long long base = (long long)blockIdx.x * 16 * PRE_ROWS + (threadIdx.x >> 4);
+  uint4 ov[PRE_ROWS], gv[PRE_ROWS];
+  float lz[PRE_ROWS];
+  long long pr[PRE_ROWS];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc += a[k] * g[k];
+  for (int k = 0; k < PRE_ROWS; ++k) {
+    const long long row = base + 16 * k;
+    ov[k] = gv[k] = make_uint4(0u, 0u, 0u, 0u);
+    lz[k] = 0.f;
+    pr[k] = -1;
+    if (row < rows) {
+      ov[k] = *reinterpret_cast<const uint4*>(o + row * 128 + 8 * sub);
+      gv[k] = *reinterpret_cast<const uint4*>(d_o + row * 128 + 8 * sub);
+      if (sub == 0) {
+        const int h = (int)(row % H);
+        const long long tok = row / H;
+        const int b = (int)(tok / S), s = (int)(tok % S);
+        pr[k] = ((long long)b * H + h) * s_pad + s;
+        lz[k] = lse[((long long)b * H + h) * S + s];
+      }
+    }
   }
 #pragma unroll
-  for (int m = 8; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (ok && sub == 0) {
-    const int h = (int)(row % H);
-    const long long tok = row / H;
-    const int b = (int)(tok / S), s = (int)(tok % S);
-    const long long pr = ((long long)b * H + h) * s_pad + s;
-    delta[pr] = acc;
-    lse2[pr] = lse[((long long)b * H + h) * S + s] * 1.4426950408889634f;
+  for (int k = 0; k < PRE_ROWS; ++k) {
+    float a[8], g[8];
+    bf16x8_to_f32(ov[k], a);
+    bf16x8_to_f32(gv[k], g);
+    float acc = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc += a[j] * g[j];
+#pragma unroll
+    for (int m = 8; m > 0; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (pr[k] >= 0) {
+      delta[pr[k]] = acc;
+      lse2[pr[k]] = lz[k] * 1.4426950408889634f;
+    }
   }
 }
 
@@ -448,15 +469,29 @@ __global__ void __launch_bounds__(256) norm_bwd_v_kernel(
   for (long long tok = (long long)blockIdx.x * WARPS + warp; tok < tokens;
        tok += (long long)gridDim.x * WARPS) {
     const __nv_bfloat16* crow = c + tok * 576;
+    // all loads first: the latent and dL rows, the row statistics and the
+    // first KP_PRE heads' k_pe gradients, so their latencies overlap
+    uint4 cv[2];
+    float dv[2][8];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      cv[hh] = *reinterpret_cast<const uint4*>(crow + 256 * hh + 8 * lane);
+      load_f32x8(dL + tok * 512 + 256 * hh + 8 * lane, dv[hh]);
+    }
     const float mu = mean[tok], rs = rstd[tok];
+    constexpr int KP_PRE = 16;
+    float2 kp[KP_PRE];
+#pragma unroll
+    for (int h = 0; h < KP_PRE; ++h)
+      kp[h] = h < H ? *reinterpret_cast<const float2*>(dkpe_h + (tok * H + h) * 64 + 2 * lane)
+                    : make_float2(0.f, 0.f);
     float xh[2][8], g[2][8];
     float s1 = 0.f, s2 = 0.f;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      const int col = 256 * hh + 8 * lane;
-      float xv[8], d[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(crow + col), xv);
-      load_f32x8(dL + tok * 512 + col, d);
+      float xv[8];
+      const float* d = dv[hh];
+      bf16x8_to_f32(cv[hh], xv);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         xh[hh][k] = (xv[k] - mu) * rs;
@@ -478,8 +513,16 @@ __global__ void __launch_bounds__(256) norm_bwd_v_kernel(
       *reinterpret_cast<float4*>(dst + 4) = make_float4(r[4], r[5], r[6], r[7]);
     }
     // sum over heads of the per-head k_pe gradient, columns 2*lane, 2*lane+1
+    // (in head order)
     float2 a = make_float2(0.f, 0.f);
-    for (int h = 0; h < H; ++h) {
+#pragma unroll
+    for (int h = 0; h < KP_PRE; ++h) {
+      if (h < H) {
+        a.x += kp[h].x;
+        a.y += kp[h].y;
+      }
+    }
+    for (int h = KP_PRE; h < H; ++h) {
       const float2 v = *reinterpret_cast<const float2*>(dkpe_h + (tok * H + h) * 64 + 2 * lane);
       a.x += v.x;
       a.y += v.y;
@@ -581,7 +624,7 @@ cudaError_t launch_bwd_pre(const Plan& p, const Ptrs& x, cudaStream_t st) {
   __nv_bfloat16* dop = p.canonical ? nullptr : x.buf<__nv_bfloat16>(p, T_DOC);
   float* lse2 = x.buf<float>(p, T_LSE2);
   if (p.canonical)
-    bwd_pre_v_kernel<<<grid_for(p.rows(), 16), 256, 0, st>>>(
+    bwd_pre_v_kernel<<<grid_for(p.rows(), 16 * PRE_ROWS), 256, 0, st>>>(
         (const __nv_bfloat16*)x.o, (const __nv_bfloat16*)x.d_o, p.S, p.H, p.rows(), delta,
         x.lse, lse2, (int)p.s_pad());
   else if (p.fp32)
