@@ -35,16 +35,23 @@ using namespace sm100;
 // instead of 48 KB for a lone 128 x 256 tile.  The pairs are persistent (one
 // per two SMs, walking the tiles in a fixed stride) and keep two accumulators,
 // so one tile's epilogue drains while the next tile's MMAs run.
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 5;   // per CTA rows; per pair columns
+constexpr int BM = 128, BN = 256, BK = 64;   // per CTA rows; per pair columns
 constexpr int BN_CTA = BN / 2;
 constexpr int A_BYTES = BM * BK * 2;       // 16 KB
 constexpr int B_BYTES = BN_CTA * BK * 2;   // 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int RING_BYTES = STAGES * STAGE_BYTES;
 constexpr int EPI_BOX = 32 * 128;          // one 32-row x 128-byte store box
-constexpr int EPI_BUFS = 4;                // store boxes in flight per epilogue warp
-constexpr int EPI_BYTES = 4 * EPI_BUFS * EPI_BOX;
-constexpr int SMEM_BYTES = RING_BYTES + EPI_BYTES + 1024;
+constexpr int SMEM_BYTES = 5 * STAGE_BYTES + 4 * 4 * EPI_BOX + 1024;
+// Ring stages and store slots per epilogue warp in those bytes: UP has a
+// short K loop and a busy epilogue (5 stages, 4 slots); DL and DW drain an
+// accumulator rarely and wait on operand loads more (6 stages, 2 slots).
+template <int MODE>
+struct Shape {
+  static constexpr int STAGES = MODE == 0 ? 5 : 6;
+  static constexpr int EPI_BUFS = MODE == 0 ? 4 : 2;
+  static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+  static_assert(RING_BYTES + 4 * EPI_BUFS * EPI_BOX + 1024 <= SMEM_BYTES, "shared memory");
+};
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 2 * BN;          // two 256-column accumulators
 constexpr int BOX8K = 64 * 64 * 2;
@@ -133,12 +140,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
   // full: rank 0's, counts both CTAs' bytes; empty: each CTA's, freed by the
   // pair MMAs' commit; acc_full: each CTA's, one accumulator complete;
   // acc_empty: rank 0's, one arrival per epilogue warp of either CTA
+  constexpr int STAGES = Shape<MODE>::STAGES, EPI_BUFS = Shape<MODE>::EPI_BUFS;
+  constexpr int RING_BYTES = Shape<MODE>::RING_BYTES;
   __shared__ uint64_t bar_full[STAGES], bar_empty[STAGES], bar_acc_full[2], bar_acc_empty[2];
   __shared__ uint32_t tmem_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_ctarank();   // = blockIdx.x & 1
   const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
 
+  if (threadIdx.x == 32) {
+    tma_prefetch_desc(&tm.a);
+    tma_prefetch_desc(&tm.b);
+    tma_prefetch_desc(&tm.o);
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(&bar_full[i], 1);
