@@ -238,13 +238,34 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(
   }
 }
 
-__global__ void dgamma_reduce_kernel(const float* __restrict__ part, int nparts, int dkv,
-                                     float* __restrict__ dgamma) {
-  int col = blockIdx.x * blockDim.x + threadIdx.x;
-  if (col >= dkv) return;
+// dgamma[col] = sum over the NGP partial rows, in a fixed order: warp w of a
+// block sums its contiguous chunk of rows in row order (all loads issued
+// first), then the chunk sums are added in warp order.  32 columns per block.
+constexpr int DG_WARPS = 16, DG_CHUNK = 32;
+static_assert(NGP <= DG_WARPS * DG_CHUNK, "dgamma chunks");
+__global__ void __launch_bounds__(DG_WARPS * 32) dgamma_reduce_kernel(
+    const float* __restrict__ part, int nparts, int dkv, float* __restrict__ dgamma) {
+  __shared__ float red[DG_WARPS][32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int col = blockIdx.x * 32 + lane;
+  const int per = (nparts + DG_WARPS - 1) / DG_WARPS;
+  const int p0 = warp * per, cnt = max(0, min(per, nparts - p0));
+  float v[DG_CHUNK];
+#pragma unroll
+  for (int i = 0; i < DG_CHUNK; ++i)
+    v[i] = (col < dkv && i < cnt) ? part[(long long)(p0 + i) * 512 + col] : 0.f;
   float t = 0.f;
-  for (int p = 0; p < nparts; ++p) t += part[(long long)p * 512 + col];
-  dgamma[col] = t;
+#pragma unroll
+  for (int i = 0; i < DG_CHUNK; ++i)
+    if (i < cnt) t += v[i];
+  red[warp][lane] = t;
+  __syncthreads();
+  if (warp == 0 && col < dkv) {
+    float s = 0.f;
+#pragma unroll
+    for (int w = 0; w < DG_WARPS; ++w) s += red[w][lane];
+    dgamma[col] = s;
+  }
 }
 
 __global__ void __launch_bounds__(256) unpad_dw_kernel(const float* __restrict__ dwc, int H, int dn,
@@ -676,7 +697,7 @@ cudaError_t launch_norm_bwd(const Plan& p, const Ptrs& x, const float* dL, cudaS
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   LaunchScope ls2_("dgamma_reduce", st);
-  dgamma_reduce_kernel<<<(p.dkv + 127) / 128, 128, 0, st>>>(part, NGP, p.dkv, x.dgamma);
+  dgamma_reduce_kernel<<<(p.dkv + 31) / 32, DG_WARPS * 32, 0, st>>>(part, NGP, p.dkv, x.dgamma);
   return cudaGetLastError();
 }
 
