@@ -4,14 +4,15 @@
 //   UP   KV[t, h, :]  = L[t, :] . W[:, h*256 : h*256+256]        M=tokens N=256/head K=512
 //   DL   dL[t, :]     = sum_h dKV[t, h, :] . W[:, h-cols]^T       M=tokens N=512      K=H*256
 //   DW   dW[:, h-cols] = sum_t L[t, :]^T dKV[t, h, :]             M=512    N=256/head K=tokens
-// One pair of CTAs (a two-CTA cluster, cta_group::2) per 256 x 256 output
-// tile, two CTAs per SM (each one's prologue and epilogue overlap the other's
-// main loop); 6 warps: warp 0 TMA producer (3-stage ring of this CTA's 128 A
-// rows and 128 B columns), warp 1 TMEM allocator and, in rank 0, the MMA
-// issuer (M256 N256 K16 pair steps, fp32 accumulator in 256 TMEM columns of
-// each CTA), warps 2-5 epilogue (TMEM -> registers -> swizzled tiles in the
-// idle ring -> TMA tensor stores).  DW splits the token reduction into a
-// fixed number of chunks whose
+// Persistent pairs of CTAs (two-CTA clusters, cta_group::2), one pair per
+// two SMs, each walking 256 x 256 output tiles in a fixed stride; 6 warps:
+// warp 0 TMA producer (a ring of this CTA's 128 A rows and 128 B columns per
+// 64-wide K step), warp 1 TMEM allocator and, in rank 0, the MMA issuer (M256
+// N256 K16 pair steps into one of two 256-column fp32 accumulators in each
+// CTA's TMEM), warps 2-5 epilogue (TMEM -> registers -> swizzled 32-row boxes
+// in per-warp store slots -> TMA tensor stores), draining one accumulator
+// while the MMAs fill the other.  DW splits the token reduction into a fixed
+// number of chunks whose
 // fp32 partial tiles are summed afterwards in chunk order, so every run adds
 // in the same order.  Each output element is one accumulation over K in
 // ascending K-step order whatever the K/V layout, which keeps the
