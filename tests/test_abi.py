@@ -51,6 +51,25 @@ def test_workspace_plan_and_tensor_listing(lib):
     assert lib.workspace_bytes(lib.make_dims(0, 16), lib.WS_SAVED) == 0
 
 
+def test_backward_scratch_listing_and_dw_split_partials(lib):
+    """The backward scratch is laid out like the saved workspace (ordered,
+    1024-aligned, inside the reported size); the dW token-split partials, when
+    present, are a whole number (2..8) of the shard's fp32 dW."""
+    for S, H, B in [(16384, 16, 1), (2048, 8, 1), (4096, 128, 1), (129, 3, 2), (1, 1, 1)]:
+        d = lib.make_dims(S, H, B=B)
+        bwd = lib.workspace_bytes(d, lib.WS_BWD)
+        ts = lib.workspace_tensors(d, lib.WS_BWD)
+        assert bwd > 0 and ts
+        for (_, off, nb), (_, off2, _) in zip(ts, ts[1:]):
+            assert off + nb <= off2 and off2 % 1024 == 0
+        assert ts[-1][1] + ts[-1][2] <= bwd
+        sizes = dict((n, b) for n, _, b in ts)
+        dw_shard = 512 * H * 256 * 4
+        if "dw_split_partials" in sizes:
+            k, rem = divmod(sizes["dw_split_partials"], dw_shard)
+            assert rem == 0 and 2 <= k <= 8, (S, H, B, k)
+
+
 def test_absorbed_minus_laga_saved_bytes_equal_closed_form(lib):
     """The form-specific activations differ by the pages' mechanism: two
     n_h*d_kv intermediates per token (absorbed) versus per-head K/V (LAGA)."""
