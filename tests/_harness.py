@@ -15,7 +15,7 @@ from laga_inputs import Workload, as_f64, make_inputs
 O_MAX_ABS = 1e-2
 O_REL_FRO = 5e-3
 GRAD_REL_FRO = 1e-2
-LSE_MAX_ABS = 2e-2
+LSE_MAX_ABS = 1e-2
 
 
 def rel_fro(x, y):
@@ -67,18 +67,61 @@ def oracle_dims(wl: Workload):
                        d_kv=wl.d_kv, B=wl.B, n_h_total=wl.n_h_total, head_offset=wl.head_offset)
 
 
-def oracle_run(wl: Workload, cpu=None, heads=None):
+def _bf16(x):
+    """Round fp64 values to the nearest bf16 (ties to even) and back."""
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16).double().numpy()
+
+
+def storage_emulated_forward(st, wl: Workload, heads=None, block=512):
+    """O of the oracle's attention recomputed in fp64 from the intermediates
+    rounded to bf16 as the library stores them: the normalised latent L, K/V
+    = bf16(L W), the RoPE'd k_pe and q_rope (and, for fp32 I/O, q_nope and
+    W_kv_b, which the library rounds to bf16 on entry).  Everything else --
+    scores, softmax, the P.V sum -- is exact.  |O_st - O| is therefore the
+    error that bf16 storage of the operands alone causes (the reading of
+    the workload's "bf16 inputs with fp32 accumulation" taken by the
+    library), element by element; no value here comes from the CUDA path."""
+    L = _bf16(st["L"])
+    W = st["W"] if wl.dtype == "bf16" else _bf16(st["W"])
+    qn = st["q_nope"] if wl.dtype == "bf16" else _bf16(st["q_nope"])
+    qr, kr = _bf16(st["q_rope_r"]), _bf16(st["kpe_r"])
+    sc = 1.0 / np.sqrt(wl.d_qk)
+    B, S = wl.B, wl.S
+    O = np.full((B, S, wl.H, wl.d_v), np.nan)
+    for h in (range(wl.H) if heads is None else heads):
+        kv = _bf16(np.einsum("bsk,kd->bsd", L, W[:, h], optimize=True))
+        k, v = kv[..., :wl.d_nope], kv[..., wl.d_nope:]
+        for b in range(B):
+            for r0 in range(0, S, block):
+                r1 = min(S, r0 + block)
+                s = (qn[b, r0:r1, h] @ k[b, :r1].T + qr[b, r0:r1, h] @ kr[b, :r1].T) * sc
+                s[np.arange(r1)[None, :] > np.arange(r0, r1)[:, None]] = -np.inf
+                p = np.exp(s - s.max(axis=1, keepdims=True))
+                O[b, r0:r1, h] = (p / p.sum(axis=1, keepdims=True)) @ v[b, :r1]
+    return O
+
+
+def oracle_run(wl: Workload, cpu=None, heads=None, storage=True):
     cpu = make_inputs(wl) if cpu is None else cpu
     a = {k: as_f64(v) for k, v in cpu.items()}
     d = oracle_dims(wl)
     O, LSE, st = oracle.forward(a["q"], a["c"], a["w"], a["gamma"], a["cos"], a["sin"], d,
                                 heads=heads)
     g = oracle.backward(st, a["dO"])
-    vmax = running_vmax(st["KV"][..., wl.d_nope:])
     # max over tokens j <= i and latent columns of |L_j|, broadcast to [B, S, 1, 1]
     lmax = np.maximum.accumulate(np.abs(st["L"]).max(axis=-1), axis=1)[:, :, None, None]
-    return dict(O=O, LSE=LSE, dq=g["dq"], dc=g["dc"], dw=g["dw"], dgamma=g["dgamma"], vmax=vmax,
-                lmax=lmax)
+    out = dict(O=O, LSE=LSE, dq=g["dq"], dc=g["dc"], dw=g["dw"], dgamma=g["dgamma"], lmax=lmax)
+    if wl.S == 1:
+        # One token: dS = P (dP - delta) with dP = dO.v = dO.O = delta, so dq
+        # vanishes by cancellation.  Its scale is that of the cancelling
+        # terms, scale * (|dP| + |delta|) * |(k_nope, k_pe)| per (b, h).
+        dl = np.abs((a["dO"] * O).sum(-1))[:, 0]                       # [B, H]
+        kn = np.linalg.norm(st["KV"][:, 0, :, :wl.d_nope], axis=-1) ** 2  # [B, H]
+        kr = np.linalg.norm(st["kpe_r"][:, 0], axis=-1)[:, None] ** 2
+        out["dq_scale"] = float(np.sqrt((((2 * dl / np.sqrt(wl.d_qk)) ** 2) * (kn + kr)).sum()))
+    if storage:
+        out["O_st"] = storage_emulated_forward(st, wl, heads)
+    return out
 
 
 def bf16_ulp(x):
@@ -87,56 +130,88 @@ def bf16_ulp(x):
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
 
 
-def o_abs_bound(Or, vmax):
-    """Per-element max-abs bound on O: 1e-2, except where bf16 storage alone
-    cannot resolve 1e-2.  O_i is a convex combination of the v_j (j <= i),
-    which are stored in bf16 (half an ulp of |v_j|) and computed from the
-    bf16-rounded normalised latent (about another half ulp); O is rounded
-    to bf16 on output (half an ulp of |O|).  ``vmax`` is max_{j<=i} |v_jd|
-    from the oracle, so the bound is max(1e-2, ulp(vmax) + ulp(|O|)/2)."""
-    return np.maximum(O_MAX_ABS, bf16_ulp(vmax) + 0.5 * bf16_ulp(Or))
+# Achieved errors of every check in this session, printed at the end of the
+# run (tests/conftest.py) so that the margin to each tolerance is visible.
+RECORDS: list = []
 
 
-def running_vmax(v):
-    """max over keys j <= i of |v[b, j, h, d]| (v: [B, S, H, d_v])."""
-    return np.maximum.accumulate(np.abs(v), axis=1)
+def _record(where, **kv):
+    RECORDS.append((where, kv))
 
 
 def check_forward(got, ref, where="", form="laga"):
-    """O max-abs (per-element bound below), O relative Frobenius, LSE max-abs.
+    """O and LSE against the oracle.
 
-    The absorbed form stores one more intermediate in bf16: the latent
-    accumulator o_lat_i, a convex combination of the L_j (j <= i), before
-    the un-absorb product.  Its bound adds one bf16 ulp of the largest |L|
-    the row averages (``lmax``)."""
+    Asserted: O relative Frobenius <= 5e-3; LSE max-abs <= 1e-2; and per
+    element |O - O_ref| <= 1e-2 + |O_st - O_ref|, i.e. the flat 1e-2 max-abs
+    target plus exactly the error that bf16 storage of L, K/V, k_pe and
+    q_rope already causes at that element (``storage_emulated_forward``).
+    The flat target alone is evaluated and recorded (elements over it, the
+    worst one and where it lies) but not asserted: bf16 storage by itself
+    moves some early-row outputs (averages of a few v's with |v| ~ 2-4, one
+    bf16 ulp = 0.016-0.031) by more than 1e-2.  The absorbed form stores the
+    latent accumulator o_lat_i, a convex combination of the L_j (j <= i), in
+    bf16 instead of K/V; its bound adds one bf16 ulp of the largest |L| the
+    row averages (``lmax``)."""
     O, Or = as_f64(got["O"]), ref["O"]
-    bound = o_abs_bound(Or, ref["vmax"])
+    err = np.abs(O - Or)
+    storage = np.abs(ref["O_st"] - Or)
+    bound = O_MAX_ABS + storage
     if form == "absorbed":
         bound = bound + bf16_ulp(ref["lmax"])
-    excess = np.abs(O - Or) - bound
-    assert excess.max() <= 0, (f"{where} O max-abs {max_abs(O, Or):.3e} exceeds its bound by "
-                               f"{excess.max():.3e}")
-    assert rel_fro(O, Or) <= O_REL_FRO, f"{where} O rel-fro {rel_fro(O, Or):.3e}"
+    worst = np.unravel_index(np.nanargmax(err), err.shape)
     L, Lr = as_f64(got["LSE"]), ref["LSE"]
-    assert max_abs(L, Lr) <= LSE_MAX_ABS, f"{where} LSE max-abs {max_abs(L, Lr):.3e}"
+    rec = dict(o_max_abs=float(np.nanmax(err)), o_flat_over=int((err > O_MAX_ABS).sum()),
+               o_n=int(err.size), o_worst_bsh=tuple(int(x) for x in worst[:3]),
+               o_storage_at_worst=float(storage[worst]),
+               o_bound_use=float(np.nanmax(err / bound)),
+               o_remainder=float(np.nanmax(np.abs(O - ref["O_st"]))),
+               o_rel_fro=rel_fro(O, Or), lse_max_abs=max_abs(L, Lr))
+    _record(where, **rec)
+    assert (err <= bound).all(), (f"{where} O max-abs {rec['o_max_abs']:.3e} exceeds 1e-2 + its "
+                                  f"storage error ({rec['o_bound_use']:.2f} of the bound)")
+    assert rec["o_rel_fro"] <= O_REL_FRO, f"{where} O rel-fro {rec['o_rel_fro']:.3e}"
+    assert rec["lse_max_abs"] <= LSE_MAX_ABS, f"{where} LSE max-abs {rec['lse_max_abs']:.3e}"
 
 
+# A reference gradient whose RMS is below this is taken as vanishing (one
+# token: dS = dO.v - dO.O = 0, so dq is zero up to fp64 rounding); only
+# then is the relative bound replaced by an absolute one.
+GRAD_VANISH_RMS = 1e-8
 GRAD_ABS_RMS = 1e-4
 
 
 def check_grads(got, ref, keys=("dq", "dc", "dw", "dgamma"), where=""):
-    """Relative Frobenius error <= 1e-2, with an absolute floor of 1e-4 RMS
-    per element for references that vanish (one token: dS = dO.v - dO.O = 0
-    exactly, so dq is identically zero)."""
+    """Relative Frobenius error <= 1e-2 for each gradient.  A reference that
+    vanishes (RMS < 1e-8) vanishes by cancellation; its error norm is held
+    to 1e-2 of the norm of the cancelling terms (``<key>_scale``), else to
+    an absolute RMS of 1e-4."""
+    errs = {}
     for k in keys:
         g, r = as_f64(got[k]), ref[k]
         err = float(np.linalg.norm(g - r))
-        lim = GRAD_REL_FRO * float(np.linalg.norm(r)) + GRAD_ABS_RMS * np.sqrt(r.size)
-        assert err <= lim, f"{where} {k} rel-fro {rel_fro(g, r):.3e} (abs {err:.3e} > {lim:.3e})"
+        rn = float(np.linalg.norm(r))
+        if rn <= GRAD_VANISH_RMS * np.sqrt(r.size):
+            if k + "_scale" in ref:
+                errs[k + "_vs_cancelling_terms"] = err / ref[k + "_scale"]
+                assert err <= GRAD_REL_FRO * ref[k + "_scale"], (
+                    f"{where} {k}: error norm {err:.3e} vs cancelling terms {ref[k + '_scale']:.3e}")
+            else:
+                errs[k + "_abs_rms"] = err / np.sqrt(r.size)
+                assert err <= GRAD_ABS_RMS * np.sqrt(r.size), (
+                    f"{where} {k} abs rms {err / np.sqrt(r.size):.3e}")
+        else:
+            errs[k] = err / rn
+            assert err <= GRAD_REL_FRO * rn, f"{where} {k} rel-fro {err / rn:.3e}"
+    _record(where, **errs)
 
 
-def head_slice(x, h, axis):
-    return np.take(x, [h], axis=axis)
+def head_view(got, ref, h):
+    """The outputs of head h alone (O, LSE and the storage-emulated O)."""
+    g = dict(O=got["O"][:, :, h], LSE=got["LSE"][:, h])
+    r = dict(O=ref["O"][:, :, h], LSE=ref["LSE"][:, h], O_st=ref["O_st"][:, :, h],
+             lmax=ref["lmax"][:, :, 0])
+    return g, r
 
 
 def dw_cols(wl: Workload, h):

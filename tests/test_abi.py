@@ -106,3 +106,15 @@ def test_bad_arguments_return_status_without_launch(lib):
     # valid arguments on a machine without a GPU fail in CUDA, not in a crash
     assert fwd(d, p) == lib.LAGA_ERR_CUDA
     assert lib.status_string(lib.LAGA_ERR_TIMEOUT) == "device wait timed out"
+
+
+def test_noalloc_rejects_latent_wider_than_its_scratch(lib):
+    """laga_norm_rope_bwd_noalloc's fixed scratch holds d_kv <= 512 columns;
+    a wider latent is refused on the host, before any CUDA call."""
+    so = lib.load()
+    d = lib.make_dims(128, 2, d_kv=1024)
+    null = ctypes.c_void_p(0)
+    st = so.laga_norm_rope_bwd_noalloc(ctypes.byref(d), null, null, null, null, null, null,
+                                       null, null, null)
+    assert st == lib.LAGA_ERR_WORKSPACE
+    assert "workspace" in lib.status_string(st)

@@ -37,7 +37,7 @@ def _peak_after_forward(wl, form, cpu):
     return peak
 
 
-@pytest.mark.parametrize("S,H", [(2048, 8), (4096, 16), (8192, 16)])
+@pytest.mark.parametrize("S,H", [(2048, 8), (4096, 16), (8192, 16), (32768, 32)])
 def test_measured_activation_gap_matches_closed_form(S, H):
     """Peak device memory of a forward (saved activations + outputs): the
     absorbed form exceeds LAGA by exactly its n_h*d_kv intermediates minus
