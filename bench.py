@@ -58,6 +58,12 @@ def parse_args():
     ap.add_argument("--sweep-S", default="2048,4096,8192,16384,32768")
     ap.add_argument("--sweep-H", default="8,16,32")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mma-rates", action="store_true",
+                    help="tensor-core issue rate per MMA shape and accumulator interleaving "
+                         "(laga_diag_mma_rate), one JSON line per case")
+    ap.add_argument("--single-stream", action="store_true",
+                    help="laga_bwd on the compute stream alone instead of laga_bwd_overlap "
+                         "(dQ kernel on a second stream of the caller's)")
     return ap.parse_args()
 
 
@@ -341,6 +347,7 @@ def run_ours(args, rank, world, local_rank):
     dg = torch.empty(512, dtype=f32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
+    aux = None if args.single_stream else torch.cuda.Stream(dev)
 
     launches = [0]
 
@@ -349,7 +356,7 @@ def run_ours(args, rank, world, local_rank):
         run.forward(tt["q"], tt["c"], tt["w"], tt["gamma"], tt["cos"], tt["sin"], o_, lse_)
         n = pkg._lib.last_launch_count()
         run.backward(tt["q"], tt["c"], tt["w"], tt["gamma"], tt["cos"], tt["sin"], o_, lse_,
-                     tt["dO"], dq_, dc_, dw_, dg_)
+                     tt["dO"], dq_, dc_, dw_, dg_, aux_stream=aux)
         launches[0] = n + pkg._lib.last_launch_count()
 
     for _ in range(args.warmup):
@@ -445,7 +452,10 @@ def run_ours(args, rank, world, local_rank):
                        "d_nope": 128, "d_rope": 64, "d_v": 128, "d_kv": 512, "form": args.form,
                        "parallelism": f"{world} independent head shards (no data-path collective)",
                        "l2": "flushed between steps by a 512 MB write outside the timed events",
-                       "value_definition": "H*S^2*1152 attention FLOPs / full hot-path step time"},
+                       "value_definition": "H*S^2*1152 attention FLOPs / full hot-path step time",
+                       "backward_call": ("laga_bwd (one stream)" if aux is None else
+                                         "laga_bwd_overlap (dQ kernel on a second caller "
+                                         "stream)")},
             "pct_of_bf16_peak": round(100 * value / world / peak_tf, 2),
             # the same work counted over the exact S(S+1)/2 causal pairs
             "value_exact_causal_pairs": round(value * (S + 1) / S, 3),
@@ -513,8 +523,56 @@ def run_sweep(args):
                 torch.cuda.empty_cache()
 
 
+# ----------------------------------------------------------------- MMA rates
+def run_mma_rates():
+    """SM clocks per tcgen05.mma (M=128, K=16, bf16 -> fp32) on every SM, by
+    N, operand form and accumulator interleaving; the peak per-SM rate the
+    measured bf16 GEMM peak implies is printed beside them."""
+    import torch
+    import sequence_latent_norm_gb300 as pkg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    n_sm = torch.cuda.get_device_properties(dev).multi_processor_count
+    cyc = torch.zeros(n_sm, dtype=torch.int64, device=dev)
+    peak_tf, _, src = measured_peaks()
+    forms = {0: "ss", 1: "ts", 2: "ss/ts alternating"}
+    n_instr = 8160
+    cases = []
+    for n in (64, 128, 192, 256):
+        for form in (0, 1, 2):
+            for n_acc, run in ((1, 1), (2, 1), (2, 4), (3, 1), (4, 1)):
+                if n_acc * n > (512 if form == 0 else 496):
+                    continue
+                cases.append((form, n, n_acc, run))
+    for form, n, n_acc, run in cases:
+        for rep in range(2):           # the first launch warms clocks and caches
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            pkg._lib.diag_mma_rate(form, n, n_acc, run, n_instr, n_sm, cyc.data_ptr())
+            b.record()
+            torch.cuda.synchronize(dev)
+        c = cyc.cpu().double()
+        if (c == 0).any():
+            raise RuntimeError("laga_diag_mma_rate: a bounded wait gave up")
+        clk = float(c.median()) / n_instr
+        flop = 2.0 * 128 * n * 16
+        # cross-check of the clock count: the launch's FLOPs over its event time
+        tflops = n_sm * n_instr * flop / (a.elapsed_time(b) * 1e-3) / 1e12
+        print(json.dumps({"mma_rate": {"form": forms[form], "N": n, "accumulators": n_acc,
+                                       "run": run, "clk_per_mma": round(clk, 1),
+                                       "flop_per_clk_per_sm": round(flop / clk),
+                                       "launch_tflops": round(tflops, 1),
+                                       "sms": n_sm, "mmas_per_sm": n_instr}}), flush=True)
+    print(json.dumps({"mma_rate_reference": {
+        "measured_bf16_peak_tflops": peak_tf, "peak_source": src,
+        "flop_per_clk_per_sm_at_2070_mhz": round(peak_tf * 1e12 / (n_sm * 2.07e9))}}), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.mma_rates:
+        run_mma_rates()
+        return
     if args.sweep:
         run_sweep(args)
         return

@@ -33,10 +33,9 @@
  * memory, never frees and never synchronises (except laga_sync_check); every
  * call only validates its arguments on the host and enqueues kernels on
  * `stream` (a cudaStream_t passed as void*, NULL = legacy default stream).
- * The one exception to single-stream execution is laga_bwd (below), which
- * forks part of its work onto a library-owned side stream and joins it back
- * into `stream`.  Outputs are overwritten,
- * not accumulated.  Summing the partial dc and dgamma of several head shards
+ * The library owns no stream and no event: the one entry point that uses a
+ * second stream, laga_bwd_overlap, takes it and its two events from the
+ * caller.  Outputs are overwritten, not accumulated.  Summing the partial dc and dgamma of several head shards
  * is the caller's job (the reduce-scatter / all-reduce of Section 5.2).
  *
  * Errors.  All argument, size and alignment checks happen before the first
@@ -136,22 +135,37 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
  *   dgamma [d_kv] fp32: this shard's partial (output)
  *   ws_saved: the forward's saved workspace (read only)
  *   ws_bwd / bwd_bytes: LAGA_WS_BWD scratch.
- * Two of the attention backward's kernels are independent.  For the LAGA
- * and explicit forms one of them runs on a side stream of the library's
- * own: one stream and two events per device, created on the first call
- * and kept for the process (so make the first call on a device outside any
- * stream capture; later calls can be captured: the fork and join are the
- * usual event record / wait pair).  The side stream forks from `stream` and joins
- * back into it with events at the end of the call, so all of the call's
- * work is ordered before anything enqueued on `stream` afterwards.  Concurrent calls on one device
- * are serialised while they enqueue.  While per-kernel profiling is enabled,
- * every kernel runs on `stream`. */
+ * Every kernel is enqueued on `stream`, in order. */
 laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
                      const float* gamma, const float* cos, const float* sin,
                      const void* o, const float* lse, const void* d_o,
                      void* dq, float* dc, float* dw, float* dgamma,
                      const void* ws_saved, size_t saved_bytes,
                      void* ws_bwd, size_t bwd_bytes, void* stream);
+
+/* laga_bwd with the two independent kernels of the attention backward on
+ * two streams, an opt-in for callers that own a second stream.  Arguments
+ * as for laga_bwd, plus:
+ *   aux_stream  a cudaStream_t of the caller's, different from `stream`
+ *   fork_event, join_event  two cudaEvent_t of the caller's (created on the
+ *               device of `stream`; timing may be disabled)
+ * The call records fork_event on `stream` and makes aux_stream wait for it;
+ * the query-stationary dQ kernel then runs on aux_stream beside the key-
+ * stationary dK/dV kernel and the up-projection and norm backward on
+ * `stream`; join_event, recorded on aux_stream after the dQ kernel, is
+ * waited on by `stream` before the call returns.  So all of the call's work
+ * is ordered before anything enqueued on `stream` afterwards, and work the
+ * caller enqueues on aux_stream afterwards follows the dQ kernel.  The
+ * events and aux_stream must not be used by another call until this one's
+ * work is enqueued (the library keeps no lock).  While per-kernel profiling
+ * is on, every kernel runs on `stream`.  For the absorbed form this is
+ * laga_bwd.  LAGA_ERR_ARG if an event is NULL or aux_stream == stream. */
+laga_status laga_bwd_overlap(const laga_dims* dims, const void* q, const void* c,
+                             const void* w_kvb, const float* gamma, const float* cos,
+                             const float* sin, const void* o, const float* lse, const void* d_o,
+                             void* dq, float* dc, float* dw, float* dgamma, const void* ws_saved,
+                             size_t saved_bytes, void* ws_bwd, size_t bwd_bytes, void* stream,
+                             void* aux_stream, void* fork_event, void* join_event);
 
 /* Synchronise `stream` and report a launch error or a device wait that gave
  * up since the last check on this device (and clear the flag). */
@@ -163,6 +177,25 @@ laga_status laga_sync_check(void* stream);
  * on this device reports LAGA_ERR_TIMEOUT.  No fault, no unbounded spin.
  * Returns LAGA_ERR_CUDA if the launch fails. */
 laga_status laga_selftest_wait_timeout(void* stream);
+
+/* Diagnostic of the tensor-core issue rate; the paper has no counterpart.
+ * Launches n_cta CTAs (one per SM when n_cta <= the SM count); in each, one
+ * thread issues n_instr tcgen05.mma of M = 128, K = 16, N = n (bf16
+ * operands, fp32 TMEM accumulator) back to back and times them with the SM
+ * clock, from the first issue to the completion of the last.
+ *   form   0: A and B in shared memory; 1: A in TMEM, B in shared memory;
+ *          2: the two alternating
+ *   n_acc, run  instruction k accumulates into accumulator (k / run) % n_acc
+ *          (n_acc = 1: one dependent chain; n_acc > 1: independent
+ *          accumulators interleaved in runs of `run` instructions)
+ *   cycles [n_cta] device array (output): SM clocks per CTA; 0 if the
+ *          bounded wait for completion gave up
+ * LAGA_ERR_ARG for n not a multiple of 16 in [16, 256], n_acc * n beyond
+ * the TMEM columns (512, or 496 when A sits in TMEM), n_instr outside
+ * [1, 2^20] or not a multiple of 48, 48 not a multiple of n_acc * run, or
+ * n_cta outside [1, 4096].  Asynchronous on `stream`. */
+laga_status laga_diag_mma_rate(int form, int n, int n_acc, int run, int n_instr, int n_cta,
+                               unsigned long long* cycles, void* stream);
 
 /* Static text for a status code. */
 const char* laga_status_string(laga_status status);

@@ -21,9 +21,9 @@ DTYPES = {"bf16": 0, "fp32": 1}
 WS_SAVED, WS_BWD = 0, 1
 
 EXPORTED = ("laga_workspace_bytes", "laga_workspace_tensor", "laga_fwd", "laga_bwd",
-            "laga_sync_check", "laga_status_string", "laga_last_launch_count",
+            "laga_bwd_overlap", "laga_sync_check", "laga_status_string", "laga_last_launch_count",
             "laga_profile_enable", "laga_profile_reset", "laga_profile_read",
-            "laga_norm_rope_bwd_noalloc", "laga_selftest_wait_timeout")
+            "laga_norm_rope_bwd_noalloc", "laga_selftest_wait_timeout", "laga_diag_mma_rate")
 
 
 class LagaDims(ctypes.Structure):
@@ -63,6 +63,9 @@ def load(path: str = LIB_PATH):
     lib.laga_fwd.restype = I
     lib.laga_bwd.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P, S, P]
     lib.laga_bwd.restype = I
+    lib.laga_bwd_overlap.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P, S, P,
+                                     P, P, P]
+    lib.laga_bwd_overlap.restype = I
     lib.laga_sync_check.argtypes = [P]
     lib.laga_sync_check.restype = I
     lib.laga_selftest_wait_timeout.argtypes = [P]
@@ -80,6 +83,8 @@ def load(path: str = LIB_PATH):
     lib.laga_profile_read.restype = I
     lib.laga_norm_rope_bwd_noalloc.argtypes = [D, P, P, P, P, P, P, P, P, P]
     lib.laga_norm_rope_bwd_noalloc.restype = I
+    lib.laga_diag_mma_rate.argtypes = [I, I, I, I, I, I, P, P]
+    lib.laga_diag_mma_rate.restype = I
     _lib = lib
     return lib
 
@@ -130,6 +135,16 @@ def bwd(dims: LagaDims, q, c, w, gamma, cos, sin, o, lse, d_o, dq, dc, dw, dgamm
                            dgamma, ws_saved, saved_bytes, ws_bwd, bwd_bytes, stream), "laga_bwd")
 
 
+def bwd_overlap(dims: LagaDims, q, c, w, gamma, cos, sin, o, lse, d_o, dq, dc, dw, dgamma,
+                ws_saved, saved_bytes, ws_bwd, bwd_bytes, stream, aux_stream, fork_event,
+                join_event):
+    """laga_bwd_overlap with raw device addresses and stream/event handles (ints)."""
+    _check(load().laga_bwd_overlap(ctypes.byref(dims), q, c, w, gamma, cos, sin, o, lse, d_o, dq,
+                                   dc, dw, dgamma, ws_saved, saved_bytes, ws_bwd, bwd_bytes,
+                                   stream, aux_stream, fork_event, join_event),
+           "laga_bwd_overlap")
+
+
 def sync_check(stream=0):
     _check(load().laga_sync_check(stream), "laga_sync_check")
 
@@ -169,3 +184,11 @@ def norm_rope_bwd_noalloc(dims: LagaDims, c, gamma, cos, sin, d_latent, d_kpe_ro
     _check(load().laga_norm_rope_bwd_noalloc(ctypes.byref(dims), c, gamma, cos, sin, d_latent,
                                              d_kpe_rot, dc, dgamma, stream),
            "laga_norm_rope_bwd_noalloc")
+
+
+def diag_mma_rate(form: int, n: int, n_acc: int, run: int, n_instr: int, n_cta: int, cycles,
+                  stream=0):
+    """laga_diag_mma_rate: SM clocks per CTA for n_instr MMAs into `cycles`
+    (a device address of n_cta uint64)."""
+    _check(load().laga_diag_mma_rate(form, n, n_acc, run, n_instr, n_cta, cycles, stream),
+           "laga_diag_mma_rate")

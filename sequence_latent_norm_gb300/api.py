@@ -121,8 +121,21 @@ class Laga:
                  p["lse"], self.ws_saved.data_ptr(), self.saved_bytes, _stream_handle(stream))
         return o, lse
 
+    def _overlap_events(self):
+        """Two events of this object for laga_bwd_overlap (created by a first
+        record, so that their handles exist)."""
+        if getattr(self, "_events", None) is None:
+            evs = (torch.cuda.Event(), torch.cuda.Event())
+            with torch.cuda.device(self.device):
+                for e in evs:
+                    e.record(torch.cuda.current_stream(self.device))
+            self._events = evs
+        return self._events
+
     def backward(self, q, c, w, gamma, cos, sin, o, lse, dO, dq=None, dc=None, dw=None,
-                 dgamma=None, stream=None):
+                 dgamma=None, stream=None, aux_stream=None):
+        """laga_bwd; with ``aux_stream`` (a torch.cuda.Stream other than the
+        compute stream) laga_bwd_overlap, which runs the dQ kernel there."""
         s = self.shard
         shp = self._shapes()
         f32 = torch.float32
@@ -132,10 +145,15 @@ class Laga:
         dgamma = torch.empty(shp["dgamma"], dtype=f32, device=self.device) if dgamma is None else dgamma
         p = self._ptrs(q=q, c=c, w=w, gamma=gamma, cos=cos, sin=sin, o=o, lse=lse, dO=dO, dq=dq,
                        dc=dc, dw=dw, dgamma=dgamma)
-        _lib.bwd(self.c_dims, p["q"], p["c"], p["w"], p["gamma"], p["cos"], p["sin"], p["o"],
-                 p["lse"], p["dO"], p["dq"], p["dc"], p["dw"], p["dgamma"],
-                 self.ws_saved.data_ptr(), self.saved_bytes, self.ws_bwd.data_ptr(),
-                 self.bwd_bytes, _stream_handle(stream))
+        args = (self.c_dims, p["q"], p["c"], p["w"], p["gamma"], p["cos"], p["sin"], p["o"],
+                p["lse"], p["dO"], p["dq"], p["dc"], p["dw"], p["dgamma"],
+                self.ws_saved.data_ptr(), self.saved_bytes, self.ws_bwd.data_ptr(),
+                self.bwd_bytes, _stream_handle(stream))
+        if aux_stream is None:
+            _lib.bwd(*args)
+        else:
+            fork, join = self._overlap_events()
+            _lib.bwd_overlap(*args, aux_stream.cuda_stream, fork.cuda_event, join.cuda_event)
         return dq, dc, dw, dgamma
 
     def workspace_tensors(self, pass_):

@@ -115,32 +115,6 @@ using namespace laga;
 // One thread waits, with a short bound (2^16 polls, ~17 ms), on an mbarrier
 // that nothing arrives on, then records the timeout code in the device error
 // word -- the same path every kernel's bounded waits take.
-// A second stream per device on which the dQ kernel runs beside the dK/dV
-// kernel (the two are independent), forked from and joined back into the
-// caller's stream with events, so the caller sees plain stream order.
-struct SideStream {
-  cudaStream_t st = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-};
-// Held while one call forks onto, and joins back from, the side stream (the
-// events are shared by all calls on a device).
-static std::mutex g_side_mu;
-static cudaError_t side_stream(SideStream** out) {
-  static SideStream per_dev[64];
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  SideStream& s = per_dev[dev];
-  if (!s.st) {
-    if ((e = cudaStreamCreateWithFlags(&s.st, cudaStreamNonBlocking)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming)) != cudaSuccess) return e;
-    if ((e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming)) != cudaSuccess) return e;
-  }
-  *out = &s;
-  return cudaSuccess;
-}
-
 static __global__ void selftest_wait_timeout_kernel(int* err) {
   __shared__ uint64_t bar;
   laga::sm100::mbar_init(&bar, 1);
@@ -218,11 +192,18 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
   return cuda_status(e);
 }
 
-laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
-                     const float* gamma, const float* cos, const float* sin, const void* o,
-                     const float* lse, const void* d_o, void* dq, float* dc, float* dw,
-                     float* dgamma, const void* ws_saved, size_t saved_bytes, void* ws_bwd,
-                     size_t bwd_bytes, void* stream) {
+// The backward of one shard.  `aux` is either `st` (everything in stream
+// order on the caller's stream) or a second stream of the caller's, forked
+// from `st` with `fork` and joined back with `join`: the dQ kernel, which
+// nothing after it reads on canonical dims, then runs beside the dK/dV
+// kernel, and the up-projection and norm backward (which need only dK/dV)
+// fill the dQ kernel's last wave.
+static laga_status bwd_impl(const laga_dims* dims, const void* q, const void* c,
+                            const void* w_kvb, const float* gamma, const float* cos,
+                            const float* sin, const void* o, const float* lse, const void* d_o,
+                            void* dq, float* dc, float* dw, float* dgamma, const void* ws_saved,
+                            size_t saved_bytes, void* ws_bwd, size_t bwd_bytes, cudaStream_t st,
+                            cudaStream_t aux, cudaEvent_t fork_ev, cudaEvent_t join_ev) {
   t_launches = 0;
   Plan p;
   laga_status s = make_plan(dims, &p);
@@ -242,17 +223,9 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
   x.ws_saved = static_cast<unsigned char*>(const_cast<void*>(ws_saved));
   x.ws_bwd = static_cast<unsigned char*>(ws_bwd);
   if ((s = err_word(&x.err)) != LAGA_OK) return s;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // dQ and dK/dV are independent, and nothing after them reads dq: dK/dV
-  // goes first on the caller's stream, dQ beside it on a side stream, so that
-  // dQ's CTAs fill dK/dV's last wave and the up-projection and norm backward
-  // (which need only dK/dV) fill dQ's.  The side stream joins back at the end
-  // (before dq_finalize where that reads dQ's rows).  With per-kernel
-  // profiling on, everything runs in turn on the caller's stream, so that
+  // With per-kernel profiling on, every kernel runs in turn on `st` so that
   // each kernel's events time it alone.
-  const bool fork = !absorbed && !g_prof_on;
-  std::unique_lock<std::mutex> lock(g_side_mu, std::defer_lock);
-  SideStream* side = nullptr;
+  const bool fork = !absorbed && aux != st && !g_prof_on;
   cudaError_t e = launch_bwd_pre(p, x, st);
   if (absorbed) {
     if (e == cudaSuccess) e = launch_absorbed_bwd(p, x, st);
@@ -260,25 +233,46 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
   } else {
     cudaStream_t dq_st = st;
     if (fork) {
-      lock.lock();
-      if (e == cudaSuccess) e = side_stream(&side);
-      if (e == cudaSuccess) e = cudaEventRecord(side->fork, st);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(side->st, side->fork, 0);
-      if (e == cudaSuccess) dq_st = side->st;
+      if (e == cudaSuccess) e = cudaEventRecord(fork_ev, st);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(aux, fork_ev, 0);
+      dq_st = aux;
     }
     if (e == cudaSuccess) e = launch_attn_bwd_kv(p, x, st);
     if (e == cudaSuccess) e = launch_attn_bwd_dq(p, x, dq_st);   // canonical: writes dq itself
-    if (fork && e == cudaSuccess) e = cudaEventRecord(side->join, side->st);
+    if (fork && e == cudaSuccess) e = cudaEventRecord(join_ev, aux);
     if (!p.canonical) {
-      if (fork && e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
+      if (fork && e == cudaSuccess) e = cudaStreamWaitEvent(st, join_ev, 0);
       if (e == cudaSuccess) e = launch_dq_finalize(p, x, st);
     }
     if (e == cudaSuccess) e = launch_upproj_bwd(p, x, st);
   }
   if (e == cudaSuccess && !p.canonical) e = launch_unpad_dw(p, x, st);
   if (e == cudaSuccess) e = launch_norm_bwd(p, x, x.buf<float>(p, T_DL), st);
-  if (fork && p.canonical && side && e == cudaSuccess) e = cudaStreamWaitEvent(st, side->join, 0);
+  if (fork && p.canonical && e == cudaSuccess) e = cudaStreamWaitEvent(st, join_ev, 0);
   return cuda_status(e);
+}
+
+laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
+                     const float* gamma, const float* cos, const float* sin, const void* o,
+                     const float* lse, const void* d_o, void* dq, float* dc, float* dw,
+                     float* dgamma, const void* ws_saved, size_t saved_bytes, void* ws_bwd,
+                     size_t bwd_bytes, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return bwd_impl(dims, q, c, w_kvb, gamma, cos, sin, o, lse, d_o, dq, dc, dw, dgamma, ws_saved,
+                  saved_bytes, ws_bwd, bwd_bytes, st, st, nullptr, nullptr);
+}
+
+laga_status laga_bwd_overlap(const laga_dims* dims, const void* q, const void* c,
+                             const void* w_kvb, const float* gamma, const float* cos,
+                             const float* sin, const void* o, const float* lse, const void* d_o,
+                             void* dq, float* dc, float* dw, float* dgamma, const void* ws_saved,
+                             size_t saved_bytes, void* ws_bwd, size_t bwd_bytes, void* stream,
+                             void* aux_stream, void* fork_event, void* join_event) {
+  if (!fork_event || !join_event || aux_stream == stream) return LAGA_ERR_ARG;
+  return bwd_impl(dims, q, c, w_kvb, gamma, cos, sin, o, lse, d_o, dq, dc, dw, dgamma, ws_saved,
+                  saved_bytes, ws_bwd, bwd_bytes, static_cast<cudaStream_t>(stream),
+                  static_cast<cudaStream_t>(aux_stream), static_cast<cudaEvent_t>(fork_event),
+                  static_cast<cudaEvent_t>(join_event));
 }
 
 laga_status laga_selftest_wait_timeout(void* stream) {

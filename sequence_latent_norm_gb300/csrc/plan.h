@@ -37,7 +37,6 @@ enum BufId {
   T_DWC,        // fp32 [512, H*256]    padded dW shard
   T_DOLAT,      // bf16 [B*S*H, 512]    dO up-projected to the latent (absorbed)
   T_DQABS,      // fp32 [B*S*H, 512]    gradient of q_absorbed (absorbed)
-  T_DLF,        // (unused)
   T_DWP,        // fp32 [splits, 512, H*256] split-K partials of dW
   N_BUF
 };
@@ -64,7 +63,7 @@ static const char* const kBufName[N_BUF] = {
     "L", "ln_mean", "ln_rstd", "k_pe_rot", "q_rope_rot", "kv", "q_absorbed", "o_latent",
     "q_nope_padded", "w_kvb_padded", "o_padded",
     "delta", "lse_log2", "dO_padded", "dq_rot", "dkv", "dk_pe_heads", "dL", "dgamma_partials",
-    "dw_padded", "dO_latent", "dq_absorbed", "dL_attention", "dw_split_partials"};
+    "dw_padded", "dO_latent", "dq_absorbed", "dw_split_partials"};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
