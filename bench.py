@@ -536,14 +536,22 @@ def run_mma_rates():
     cyc = torch.zeros(n_sm, dtype=torch.int64, device=dev)
     peak_tf, _, src = measured_peaks()
     forms = {0: "ss", 1: "ts", 2: "ss/ts alternating"}
+    bgs = {0: "none", 1: "TMEM loads", 2: "shared-memory stores", 3: "TMA bulk copies",
+           4: "TMEM stores", 5: "exp + FMA"}
     n_instr = 8160
     cases = []
     for n in (64, 128, 192, 256):
-        for form in (0, 1, 2):
-            for n_acc, run in ((1, 1), (2, 1), (2, 4), (3, 1), (4, 1)):
-                if n_acc * n > (512 if form == 0 else 496):
-                    continue
-                cases.append((form, n, n_acc, run))
+        for op in (0, 1):
+            for bmn in (0, 1):
+                for bg in (0, 1, 2):
+                    cases.append((op | (bmn << 2) | (bg << 3), n, 1, 1))
+    for op in (0, 1, 2):
+        for n_acc, run in ((2, 1), (2, 4), (3, 1)):
+            cases.append((op, 128, n_acc, run))
+    for n in (64, 128, 256):
+        for op in (0, 1):
+            for bg in (0, 1, 3, 4, 5):
+                cases.append((op | 4 | (bg << 3) | 64, n, 1, 1))
     for form, n, n_acc, run in cases:
         for rep in range(2):           # the first launch warms clocks and caches
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -558,7 +566,12 @@ def run_mma_rates():
         flop = 2.0 * 128 * n * 16
         # cross-check of the clock count: the launch's FLOPs over its event time
         tflops = n_sm * n_instr * flop / (a.elapsed_time(b) * 1e-3) / 1e12
-        print(json.dumps({"mma_rate": {"form": forms[form], "N": n, "accumulators": n_acc,
+        print(json.dumps({"mma_rate": {"form": forms[form & 3],
+                                       "b_major": "MN" if form & 4 else "K",
+                                       "background": bgs[(form >> 3) & 7],
+                                       "operands": "N(0,1)-like" if form & 64 else "small",
+                                       "N": n,
+                                       "accumulators": n_acc,
                                        "run": run, "clk_per_mma": round(clk, 1),
                                        "flop_per_clk_per_sm": round(flop / clk),
                                        "launch_tflops": round(tflops, 1),

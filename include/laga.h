@@ -183,17 +183,27 @@ laga_status laga_selftest_wait_timeout(void* stream);
  * thread issues n_instr tcgen05.mma of M = 128, K = 16, N = n (bf16
  * operands, fp32 TMEM accumulator) back to back and times them with the SM
  * clock, from the first issue to the completion of the last.
- *   form   0: A and B in shared memory; 1: A in TMEM, B in shared memory;
- *          2: the two alternating
+ *   form   bits 0-1  0: A and B in shared memory; 1: A in TMEM, B in shared
+ *                    memory; 2: the two alternating
+ *          bit 2     B MN-major (64-wide N boxes) instead of K-major
+ *          bits 3-5  while the MMAs run, the CTA's other three warps
+ *                    0: idle; 1: stream TMEM loads from other columns;
+ *                    2: stream 16-byte shared-memory stores;
+ *                    3: stream 16 KB bulk copies (TMA) into shared memory;
+ *                    4: stream TMEM stores to other columns;
+ *                    5: exponentials and FMAs in registers
+ *          bit 6     operands spread like N(0,1) draws instead of small
+ *                    repeating values
  *   n_acc, run  instruction k accumulates into accumulator (k / run) % n_acc
  *          (n_acc = 1: one dependent chain; n_acc > 1: independent
  *          accumulators interleaved in runs of `run` instructions)
  *   cycles [n_cta] device array (output): SM clocks per CTA; 0 if the
  *          bounded wait for completion gave up
- * LAGA_ERR_ARG for n not a multiple of 16 in [16, 256], n_acc * n beyond
- * the TMEM columns (512, or 496 when A sits in TMEM), n_instr outside
- * [1, 2^20] or not a multiple of 48, 48 not a multiple of n_acc * run, or
- * n_cta outside [1, 4096].  Asynchronous on `stream`. */
+ * LAGA_ERR_ARG for n not a multiple of 16 in [16, 256] (of 64 with an
+ * MN-major B), n_acc * n beyond the free TMEM columns (512; 496 with A in
+ * TMEM; 448 with background TMEM loads or stores), n_instr outside [1, 2^20] or not a
+ * multiple of 48, 48 not a multiple of n_acc * run, or n_cta outside
+ * [1, 4096].  Asynchronous on `stream`. */
 laga_status laga_diag_mma_rate(int form, int n, int n_acc, int run, int n_instr, int n_cta,
                                unsigned long long* cycles, void* stream);
 

@@ -147,23 +147,24 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       const uint32_t idS = idesc_bf16(128, 128, 0, 0);
       const uint32_t idQ = idesc_bf16(128, 192, 0, 1);
-      const uint32_t qr = smem_u32(sm + QR_OFF), ga = smem_u32(sm + DO_OFF);
-      const uint32_t va = smem_u32(sm + V_OFF);
+      const uint32_t qrlo = sdesc_lo(smem_u32(sm + QR_OFF), 16);
+      const uint32_t glo = sdesc_lo(smem_u32(sm + DO_OFF), 16);
+      const uint32_t vlo = sdesc_lo(smem_u32(sm + V_OFF), 16);
       // S_ij = Q_i K_j^T (12 K-steps over d = 192): q_nope from TMEM for
       // the first 8, q_rope from shared memory for the last 4
       auto issue_s = [&](int j) -> bool {
         if (!mbar_wait(&bar_k_full[j % K_BUFS], (j / K_BUFS) & 1, p.err)) return false;
         tc_fence_after();
-        const uint32_t ka = smem_u32(sm + K_OFF + (j % K_BUFS) * 3 * BOX);
+        const uint32_t klo = sdesc_lo(smem_u32(sm + K_OFF + (j % K_BUFS) * 3 * BOX), 16);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
-          mma_ts(tmem + C_S, tmem + C_QN + 8 * s, sdesc_sw128(ka + off, 16, 1024), idS, s > 0);
+          const uint32_t off = ((s >> 2) * BOX + (s & 3) * 32) >> 4;
+          mma_ts(tmem + C_S, tmem + C_QN + 8 * s, sdesc_make(klo + off), idS, s > 0);
         }
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          mma_ss(tmem + C_S, sdesc_sw128(qr + s * 32, 16, 1024),
-                 sdesc_sw128(ka + 2 * BOX + s * 32, 16, 1024), idS, 1u);
+          mma_ss(tmem + C_S, sdesc_make(qrlo + ((s * 32) >> 4)),
+                 sdesc_make(klo + ((2 * BOX + s * 32) >> 4)), idS, 1u);
         mma_commit(&bar_s);
         return true;
       };
@@ -173,9 +174,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
-          mma_ss(tmem + C_DP, sdesc_sw128(ga + off, 16, 1024), sdesc_sw128(va + off, 16, 1024),
-                 idS, s > 0);
+          const uint32_t off = ((s >> 2) * BOX + (s & 3) * 32) >> 4;
+          mma_ss(tmem + C_DP, sdesc_make(glo + off), sdesc_make(vlo + off), idS, s > 0);
         }
         mma_commit(&bar_dp);
         mma_commit(&bar_v_free);
@@ -190,10 +190,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // dQ += dS_ij K_j (dS from TMEM, K_j as the N-major B operand)
         if (!mbar_wait(&bar_ds, j & 1, p.err)) break;
         tc_fence_after();
-        const uint32_t ka = smem_u32(sm + K_OFF + (j % K_BUFS) * 3 * BOX);
+        const uint32_t kmn = sdesc_lo(smem_u32(sm + K_OFF + (j % K_BUFS) * 3 * BOX), BOX);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DQ, tmem + ds_col(s), sdesc_sw128(ka + s * 2048, BOX, 1024), idQ,
+          mma_ts(tmem + C_DQ, tmem + ds_col(s), sdesc_make(kmn + s * (2048 >> 4)), idQ,
                  (j > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_k_free[j % K_BUFS]);
         // dP_i,j+1 overwrites dS_ij only after the dQ MMAs above have read it

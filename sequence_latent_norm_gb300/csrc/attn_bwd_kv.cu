@@ -161,36 +161,36 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idST = idesc_bf16(128, 128, 0, 0);
       const uint32_t idMN = idesc_bf16(128, 128, 0, 1);
       const uint32_t idDKr = idesc_bf16(128, 64, 0, 1);
-      const uint32_t kb = smem_u32(sm + K_OFF), vb = smem_u32(sm + V_OFF);
-      const uint32_t gb = smem_u32(sm + DO_OFF);
+      const uint32_t klo = sdesc_lo(smem_u32(sm + K_OFF), 16);
+      const uint32_t vlo = sdesc_lo(smem_u32(sm + V_OFF), 16);
+      const uint32_t glo = sdesc_lo(smem_u32(sm + DO_OFF), 16);      // dO K-major (dP^T)
+      const uint32_t glo_mn = sdesc_lo(smem_u32(sm + DO_OFF), BOX);  // dO MN-major (dV)
       // S^T_i = K Q_i^T (12 K-steps over d = 192) into [256,384), in two
       // parts: the 8 k_nope steps, then the 4 k_pe steps and the commit
       auto issue_s_nope = [&](int t) -> bool {
         if (!mbar_wait(&bar_q_full[t & 1], (t >> 1) & 1, p.err)) return false;
         tc_fence_after();
-        const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
+        const uint32_t qlo = sdesc_lo(smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX), 16);
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
-          mma_ss(tmem + C_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                 idST, s > 0);
+          const uint32_t off = ((s >> 2) * BOX + (s & 3) * 32) >> 4;
+          mma_ss(tmem + C_S, sdesc_make(klo + off), sdesc_make(qlo + off), idST, s > 0);
         }
         return true;
       };
       auto issue_s_rope = [&](int t) {
-        const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
+        const uint32_t qlo = sdesc_lo(smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX), 16);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          const uint32_t off = 2 * BOX + s * 32;
-          mma_ss(tmem + C_S, sdesc_sw128(kb + off, 16, 1024), sdesc_sw128(qb + off, 16, 1024),
-                 idST, 1u);
+          const uint32_t off = (2 * BOX + s * 32) >> 4;
+          mma_ss(tmem + C_S, sdesc_make(klo + off), sdesc_make(qlo + off), idST, 1u);
         }
         mma_commit(&bar_s);
       };
       bool ok = mbar_wait(&bar_kv, 0, p.err) && issue_s_nope(0);
       if (ok) issue_s_rope(0);
       for (int t = 0; ok && t < n_i; ++t) {
-        const uint32_t qb = smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX);
+        const uint32_t qlo_mn = sdesc_lo(smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX), BOX);
         const bool next = t + 1 < n_i;
         // dP^T = V dO^T (8 K-steps over d_v) into [384,512): dS^T of tile
         // i-1 there was read by the dK MMAs issued before, and the k_pe part
@@ -200,9 +200,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s) {
-          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
-          mma_ss(tmem + C_DP, sdesc_sw128(vb + off, 16, 1024), sdesc_sw128(gb + off, 16, 1024),
-                 idST, s > 0);
+          const uint32_t off = ((s >> 2) * BOX + (s & 3) * 32) >> 4;
+          mma_ss(tmem + C_DP, sdesc_make(vlo + off), sdesc_make(glo + off), idST, s > 0);
         }
         mma_commit(&bar_dp);
         // dV += P^T dO (P^T from TMEM); afterwards dO_i is no longer read
@@ -210,7 +209,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DV, tmem + packed_col(C_S, s), sdesc_sw128(gb + s * 2048, BOX, 1024),
+          mma_ts(tmem + C_DV, tmem + packed_col(C_S, s), sdesc_make(glo_mn + s * (2048 >> 4)),
                  idMN, (t > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_do_free);
         // S^T_{i+1} overwrites P^T_i only after the dV MMAs above read it.
@@ -223,13 +222,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int s = 0; s < 8; ++s)
           mma_ts(tmem + C_DKR, tmem + packed_col(C_DP, s),
-                 sdesc_sw128(qb + 2 * BOX + s * 2048, BOX, 1024), idDKr, s > 0);
+                 sdesc_make(qlo_mn + ((2 * BOX + s * 2048) >> 4)), idDKr, s > 0);
         mma_commit(&bar_dkr);
         if (next) issue_s_rope(t + 1);
         // dK_nope += dS^T Q_nope
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_ts(tmem + C_DK, tmem + packed_col(C_DP, s), sdesc_sw128(qb + s * 2048, BOX, 1024),
+          mma_ts(tmem + C_DK, tmem + packed_col(C_DP, s), sdesc_make(qlo_mn + s * (2048 >> 4)),
                  idMN, (t > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_q_free[t & 1]);
       }

@@ -152,17 +152,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
       const uint32_t idO = idesc_bf16(BM, 128, 0, 1);
       const uint32_t qa = smem_u32(Qs);
+      const uint32_t qlo = sdesc_lo(qa, 16);
       bool ok = mbar_wait(&bar_q, 0, p.err);
       auto issue_s = [&](int j) -> bool {
         const int st = j & 1;
         if (!mbar_wait(&bar_kf[st], (j >> 1) & 1, p.err)) return false;
         tc_fence_after();
-        const uint32_t ka = smem_u32(Ks + st * K_BYTES);
+        const uint32_t klo = sdesc_lo(smem_u32(Ks + st * K_BYTES), 16);
         const uint32_t d = tmem + st * BN;
 #pragma unroll
         for (int s = 0; s < 12; ++s) {
-          const uint32_t off = (s >> 2) * BOX + (s & 3) * 32;
-          mma_ss(d, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), idS, s > 0);
+          const uint32_t off = ((s >> 2) * BOX + (s & 3) * 32) >> 4;
+          mma_ss(d, sdesc_make(qlo + off), sdesc_make(klo + off), idS, s > 0);
         }
         mma_commit(&bar_s[st]);
         return true;
@@ -174,12 +175,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(&bar_p[st], (j >> 1) & 1, p.err)) break;
         if (!mbar_wait(&bar_vf[st], (j >> 1) & 1, p.err)) break;
         tc_fence_after();
-        const uint32_t va = smem_u32(Vs + st * V_BYTES);
+        const uint32_t vlo = sdesc_lo(smem_u32(Vs + st * V_BYTES), BOX);
         const uint32_t pa = tmem + st * BN;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
           mma_ts(tmem + O_COL, pa + (s < 4 ? 8 * s : 64 + 8 * (s - 4)),
-                 sdesc_sw128(va + s * 2048, BOX, 1024), idO,
+                 sdesc_make(vlo + s * (2048 >> 4)), idO,
                  (j > 0 || s > 0) ? 1u : 0u);
         mma_commit(&bar_ve[st]);
       }
@@ -197,12 +198,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&bar_s[st], (j >> 1) & 1, p.err)) { ok = false; break; }
       tc_fence_after();
       float s[64];
+      {
+        uint32_t u[64];
+        tmem_ld64(tmem_addr(tmem, qd, st * BN + ch * 64), u);
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, qd, st * BN + ch * 64 + c * 32), u);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[c * 32 + k] = __uint_as_float(u[k]);
+        for (int k = 0; k < 64; ++k) s[k] = __uint_as_float(u[k]);
       }
       if (j == n_kt - 1) {  // diagonal tile: key k0+c visible iff c <= r and k0+c < S
         const int lim = min(r, p.S - 1 - j * BN) - ch * 64;

@@ -15,11 +15,15 @@ namespace {
 using namespace sm100;
 
 constexpr int A_BYTES = 128 * 128;        // 128 rows x 64 bf16 (one swizzle box)
-constexpr int B_BYTES = 256 * 128;        // up to 256 rows x 64 bf16
+constexpr int B_BYTES = 4 * 128 * 128;    // four 128-row boxes (N up to 256, either major)
+constexpr int BG_OFF = A_BYTES + B_BYTES; // shared-memory stores of the background warps
+constexpr int BG_BYTES = 32 * 1024;
 // more than half of an SM's shared memory, so that exactly one CTA runs per SM
 constexpr int SMEM = 120 * 1024;
 constexpr int A_TMEM_COL = 496;           // A operand of the TMEM form: 16 columns
+constexpr int BG_TMEM_COL = 448;          // columns the background TMEM loads read
 __device__ int g_diag_err;                // bounded waits of this diagnostic give up here
+__device__ __align__(128) uint8_t g_diag_src[64 * 1024];   // source of the background bulk copies
 
 // Instructions are issued in fully unrolled blocks of UNR (a multiple of
 // every run * n_acc pattern used), with every operand descriptor and
@@ -28,23 +32,48 @@ __device__ int g_diag_err;                // bounded waits of this diagnostic gi
 constexpr int UNR = 48;
 
 // FORM 0: A and B in shared memory; 1: A in TMEM; 2: alternating 0 and 1.
+// BMN: B is MN-major (N in 64-wide boxes 16 KB apart) instead of K-major.
+// BG: while the MMAs run, warps 1-3 0: idle; 1: stream tcgen05.ld from
+// other TMEM columns; 2: stream 16-byte shared-memory stores; 3: warp 1
+// streams 16 KB bulk copies (the TMA engine) from global into shared
+// memory, two in flight; 4: stream TMEM stores; 5: exponentials and FMAs
+// in registers.
 // Instruction k goes to accumulator (k / run) % n_acc at column acc * n.
-template <int FORM>
+template <int FORM, int BMN, int BG>
 __global__ void __launch_bounds__(128, 1)
-    diag_mma_kernel(int n, int n_acc, int run, int n_blocks, unsigned long long* cycles,
+    diag_mma_kernel(int n, int n_acc, int run, int n_blocks, int rnd, unsigned long long* cycles,
                     int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar;
+  __shared__ uint64_t bar, bg_bar[2];
   __shared__ uint32_t tmem_sh;
-  const int warp = threadIdx.x >> 5;
-  // operands: small finite bf16 values (the rate does not depend on them)
-  for (int i = threadIdx.x; i < (A_BYTES + B_BYTES) / 2; i += blockDim.x)
-    reinterpret_cast<__nv_bfloat16*>(sm)[i] = __float2bfloat16_rn(0.001f * (float)(i % 7));
+  __shared__ volatile int stop;
+  __shared__ float sink[4];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // operands: small repeating values, or (rnd) values spread like N(0,1)
+  // draws (a sum of four uniform hashes), whose bit patterns toggle like
+  // real activations
+  for (int i = threadIdx.x; i < (A_BYTES + B_BYTES) / 2; i += blockDim.x) {
+    float v = 0.001f * (float)(i % 7);
+    if (rnd) {
+      uint32_t hsh = (uint32_t)i * 2654435761u + blockIdx.x * 40503u;
+      float u = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        hsh ^= hsh >> 15; hsh *= 2246822519u; hsh ^= hsh >> 13;
+        u += (float)(hsh & 0xffffu) * (1.0f / 65536.0f);
+      }
+      v = (u - 2.0f) * 1.7320508f;
+    }
+    reinterpret_cast<__nv_bfloat16*>(sm)[i] = __float2bfloat16_rn(v);
+  }
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&bg_bar[0], 1);
+    mbar_init(&bg_bar[1], 1);
     fence_barrier_init();
+    stop = 0;
   }
   if (warp == 0) {
     tmem_alloc(&tmem_sh, 512);
@@ -58,7 +87,7 @@ __global__ void __launch_bounds__(128, 1)
   {
     uint32_t z[16];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) z[k] = 0x3c003c00u;   // bf16 pairs of small values
+    for (int k = 0; k < 16; ++k) z[k] = rnd ? 0xbf803f80u ^ (uint32_t)(k * 0x00110011u) : 0x3c003c00u;
     tmem_st16(tmem_addr(tmem, warp, A_TMEM_COL), z);
     tmem_wait_st();
   }
@@ -66,13 +95,13 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   if (threadIdx.x == 0) {
-    const uint32_t id = idesc_bf16(128, n, 0, 0);
+    const uint32_t id = idesc_bf16(128, n, 0, BMN);
     const uint32_t ab = smem_u32(sm), bb = smem_u32(sm + A_BYTES);
     uint64_t ad[4], bd[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       ad[k] = sdesc_sw128(ab + 32 * k, 16, 1024);
-      bd[k] = sdesc_sw128(bb + 32 * k, 16, 1024);
+      bd[k] = BMN ? sdesc_sw128(bb + 2048 * k, 128 * 128, 1024) : sdesc_sw128(bb + 32 * k, 16, 1024);
     }
     uint32_t d[UNR];
 #pragma unroll
@@ -93,6 +122,65 @@ __global__ void __launch_bounds__(128, 1)
     const bool ok = mbar_wait(&bar, 0, err);
     const unsigned long long t1 = clock64();
     cycles[blockIdx.x] = ok ? t1 - t0 : 0ull;
+    stop = 1;
+  } else if (BG == 3 && warp == 1) {
+    // background bulk copies until the MMAs are done (bounded)
+    if (lane == 0) {
+      uint32_t issued[2] = {0u, 0u};
+      for (uint32_t it = 0; it < (1u << 20) && !stop; ++it) {
+        const int k = it & 1;
+        if (issued[k] && !mbar_wait(&bg_bar[k], (issued[k] - 1) & 1, err)) break;
+        mbar_arrive_expect_tx(&bg_bar[k], 16384);
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            ::"r"(smem_u32(sm + BG_OFF + k * 16384)), "l"(g_diag_src + k * 16384), "r"(16384),
+            "r"(smem_u32(&bg_bar[k]))
+            : "memory");
+        ++issued[k];
+      }
+      for (int k = 0; k < 2; ++k)
+        if (issued[k]) mbar_wait(&bg_bar[k], (issued[k] - 1) & 1, err);
+    }
+  } else if (BG == 5 && warp > 0) {
+    // background exponentials and FMAs, the mix of a softmax, until the
+    // MMAs are done
+    float x[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) x[k] = 0.001f * (float)(lane + k);
+    for (uint32_t it = 0; it < (1u << 22) && !stop; ++it) {
+#pragma unroll
+      for (int k = 0; k < 16; ++k) x[k] = ex2(fmaf(x[k], -0.75f, 0.25f));
+    }
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc += x[k];
+    if (lane == 0) sink[warp] = acc;
+  } else if (BG == 4 && warp > 0) {
+    // background TMEM stores (and their completion waits) until the MMAs are done
+    uint32_t v[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = 0x3f803f80u + (uint32_t)k;
+    for (uint32_t it = 0; it < (1u << 22) && !stop; ++it) {
+      v[it & 15] += 1u;
+      tmem_st16(tmem_addr(tmem, warp, BG_TMEM_COL + (int)(it & 1) * 16), v);
+      tmem_wait_st();
+    }
+  } else if ((BG == 1 || BG == 2) && warp > 0) {
+    // background traffic until the MMAs are done (bounded)
+    float acc = 0.f;
+    for (uint32_t it = 0; it < (1u << 22) && !stop; ++it) {
+      if (BG == 1) {
+        uint32_t u[32];
+        tmem_ld32(tmem_addr(tmem, warp, BG_TMEM_COL), u);
+        acc += __uint_as_float(u[it & 31]);
+      } else {
+        uint4* dst = reinterpret_cast<uint4*>(sm + BG_OFF + (warp - 1) * 8192);
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          dst[(k * 32 + lane + (int)(it & 3) * 128) & 511] = make_uint4(it, k, lane, warp);
+      }
+    }
+    if (lane == 0) sink[warp] = acc;
   }
   tc_fence_before();
   __syncthreads();
@@ -102,14 +190,38 @@ __global__ void __launch_bounds__(128, 1)
   }
 }
 
-template <int FORM>
-cudaError_t launch_diag(int n, int n_acc, int run, int n_blocks, int n_cta,
+template <int FORM, int BMN, int BG>
+cudaError_t launch_diag(int n, int n_acc, int run, int n_blocks, int rnd, int n_cta,
                         unsigned long long* cycles, int* err, cudaStream_t st) {
-  cudaError_t e = cudaFuncSetAttribute(diag_mma_kernel<FORM>,
+  cudaError_t e = cudaFuncSetAttribute(diag_mma_kernel<FORM, BMN, BG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  diag_mma_kernel<FORM><<<n_cta, 128, SMEM, st>>>(n, n_acc, run, n_blocks, cycles, err);
+  diag_mma_kernel<FORM, BMN, BG><<<n_cta, 128, SMEM, st>>>(n, n_acc, run, n_blocks, rnd, cycles,
+                                                           err);
   return cudaGetLastError();
+}
+
+template <int FORM, int BMN>
+cudaError_t launch_diag_bg(int bg, int n, int n_acc, int run, int n_blocks, int rnd, int n_cta,
+                           unsigned long long* cycles, int* err, cudaStream_t st) {
+  if (bg == 1)
+    return launch_diag<FORM, BMN, 1>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+  if (bg == 2)
+    return launch_diag<FORM, BMN, 2>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+  if (bg == 3)
+    return launch_diag<FORM, BMN, 3>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+  if (bg == 4)
+    return launch_diag<FORM, BMN, 4>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+  if (bg == 5)
+    return launch_diag<FORM, BMN, 5>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+  return launch_diag<FORM, BMN, 0>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+}
+
+template <int FORM>
+cudaError_t launch_diag_form(int bmn, int bg, int n, int n_acc, int run, int n_blocks, int rnd,
+                             int n_cta, unsigned long long* cycles, int* err, cudaStream_t st) {
+  return bmn ? launch_diag_bg<FORM, 1>(bg, n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st)
+             : launch_diag_bg<FORM, 0>(bg, n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
 }
 
 }  // namespace
@@ -118,20 +230,23 @@ cudaError_t launch_diag(int n, int n_acc, int run, int n_blocks, int n_cta,
 extern "C" laga_status laga_diag_mma_rate(int form, int n, int n_acc, int run, int n_instr,
                                           int n_cta, unsigned long long* cycles, void* stream) {
   using namespace laga;
-  if (form < 0 || form > 2 || n < 16 || n > 256 || n % 16 != 0 || n_acc < 1 || run < 1 ||
-      n_instr < 1 || n_instr > (1 << 20) || n_cta < 1 || n_cta > 4096 || !cycles)
+  const int op = form & 3, bmn = (form >> 2) & 1, bg = (form >> 3) & 7, rnd = (form >> 6) & 1;
+  if (form < 0 || form >= 128 || bg > 5 || op > 2 || n < 16 || n > 256 || n % 16 != 0 ||
+      n_acc < 1 || run < 1 || n_instr < 1 || n_instr > (1 << 20) || n_cta < 1 || n_cta > 4096 ||
+      !cycles)
     return LAGA_ERR_ARG;
-  if (n_acc * n > (form == 0 ? 512 : A_TMEM_COL) || n_instr % UNR != 0 ||
-      UNR % (n_acc * run) != 0)
-    return LAGA_ERR_ARG;
+  if (bmn && n % 64 != 0) return LAGA_ERR_ARG;
+  const int cols = (bg == 1 || bg == 4) ? BG_TMEM_COL : (op == 0 ? 512 : A_TMEM_COL);
+  if (n_acc * n > cols || n_instr % UNR != 0 || UNR % (n_acc * run) != 0) return LAGA_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(cycles) & 7u) != 0) return LAGA_ERR_ALIGN;
   void* err = nullptr;
   if (cudaGetSymbolAddress(&err, g_diag_err) != cudaSuccess) return LAGA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int nb = n_instr / UNR;
   int* ew = static_cast<int*>(err);
-  cudaError_t e = form == 0   ? launch_diag<0>(n, n_acc, run, nb, n_cta, cycles, ew, st)
-                  : form == 1 ? launch_diag<1>(n, n_acc, run, nb, n_cta, cycles, ew, st)
-                              : launch_diag<2>(n, n_acc, run, nb, n_cta, cycles, ew, st);
+  cudaError_t e =
+      op == 0   ? launch_diag_form<0>(bmn, bg, n, n_acc, run, nb, rnd, n_cta, cycles, ew, st)
+      : op == 1 ? launch_diag_form<1>(bmn, bg, n, n_acc, run, nb, rnd, n_cta, cycles, ew, st)
+                : launch_diag_form<2>(bmn, bg, n, n_acc, run, nb, rnd, n_cta, cycles, ew, st);
   return e == cudaSuccess ? LAGA_OK : LAGA_ERR_CUDA;
 }

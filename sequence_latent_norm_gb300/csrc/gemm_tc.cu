@@ -218,12 +218,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t a = smem_u32(sm + st * STAGE_BYTES);
           const uint32_t bsm = a + A_BYTES;
+          const uint32_t alo = MODE == DW ? sdesc_lo(a, BOX8K) : sdesc_lo(a, 16);
+          const uint32_t blo = MODE == DL ? sdesc_lo(bsm, 16) : sdesc_lo(bsm, BOX8K);
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = MODE == DW ? sdesc_sw128(a + kk * 2048, BOX8K, 1024)
-                                           : sdesc_sw128(a + kk * 32, 16, 1024);
-            const uint64_t bd = MODE == DL ? sdesc_sw128(bsm + kk * 32, 16, 1024)
-                                           : sdesc_sw128(bsm + kk * 2048, BOX8K, 1024);
+            const uint64_t ad = sdesc_make(alo + (MODE == DW ? kk * (2048 >> 4) : kk * (32 >> 4)));
+            const uint64_t bd = sdesc_make(blo + (MODE == DL ? kk * (32 >> 4) : kk * (2048 >> 4)));
             mma_ss_pair(d, ad, bd, idesc, (k > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit_pair(&bar_empty[st]);
