@@ -552,6 +552,29 @@ def run_mma_rates():
         for op in (0, 1):
             for bg in (0, 1, 3, 4, 5):
                 cases.append((op | 4 | (bg << 3) | 64, n, 1, 1))
+    # how long one 32-column TMEM load (with its wait) takes while the tensor
+    # core streams MMAs into other columns
+    for n in (64, 128, 256):
+        form = 1 | 4 | (1 << 3) | 64 | 128
+        for rep in range(2):
+            pkg._lib.diag_mma_rate(form, n, 1, 1, n_instr, n_sm, cyc.data_ptr())
+            torch.cuda.synchronize(dev)
+        c = cyc.cpu().double()
+        print(json.dumps({"tmem_load_latency": {"clk_per_32_column_load": float(c.median()),
+                                                "alongside": f"ts N={n} MMAs, N(0,1)-like"}}),
+              flush=True)
+    # one dependent broadcast 16-byte shared-memory load, with the tensor
+    # core idle (a single MMA) and while it streams MMAs of each form
+    for op in (0, 1):
+        for n, instr in ((128, 48), (128, n_instr), (256, n_instr)):
+            form = op | 4 | (6 << 3) | 64 | 128
+            for rep in range(2):
+                pkg._lib.diag_mma_rate(form, n, 1, 1, instr, n_sm, cyc.data_ptr())
+                torch.cuda.synchronize(dev)
+            c = cyc.cpu().double()
+            print(json.dumps({"smem_broadcast_load_latency": {
+                "clk_per_load": float(c.median()),
+                "alongside": f"{forms[op]} N={n} MMAs x {instr}"}}), flush=True)
     for form, n, n_acc, run in cases:
         for rep in range(2):           # the first launch warms clocks and caches
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

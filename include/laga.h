@@ -191,7 +191,8 @@ laga_status laga_selftest_wait_timeout(void* stream);
  *                    2: stream 16-byte shared-memory stores;
  *                    3: stream 16 KB bulk copies (TMA) into shared memory;
  *                    4: stream TMEM stores to other columns;
- *                    5: exponentials and FMAs in registers
+ *                    5: exponentials and FMAs in registers;
+ *                    6: broadcast shared-memory loads (all lanes one address)
  *          bit 6     operands spread like N(0,1) draws instead of small
  *                    repeating values
  *   n_acc, run  instruction k accumulates into accumulator (k / run) % n_acc

@@ -267,9 +267,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(tmem_addr(tmem, qd, C_S + col0), us);
         const float4* l4 = reinterpret_cast<const float4*>(lse_s + col0);
         if (full) {
+          // all of the chunk's LSE values first: shared-memory loads wait
+          // behind the tensor core's operand reads, so none may sit between
+          // the exponentials
+          float4 lz[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) lz[k] = l4[k];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const float4 l = l4[k];
+            const float4 l = lz[k];
             pv[kk * 32 + 4 * k] = ex2(fmaf(__uint_as_float(us[4 * k]), p.sl2, -l.x));
             pv[kk * 32 + 4 * k + 1] = ex2(fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -l.y));
             pv[kk * 32 + 4 * k + 2] = ex2(fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -l.z));
@@ -304,14 +310,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int col0 = ch * 64 + c * 32;
         uint32_t ud[32], dk[16];
         tmem_ld32(tmem_addr(tmem, qd, C_DP + col0), ud);
-        const float2* d2 = reinterpret_cast<const float2*>(dlt_s + col0);
+        // all of the chunk's delta values first (see phase A)
+        const float4* d4 = reinterpret_cast<const float4*>(dlt_s + col0);
+        float4 dz[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float2 dl = d2[k];
-          const float d0 = pv[kk * 32 + 2 * k] * (__uint_as_float(ud[2 * k]) - dl.x) * p.scale;
-          const float d1 =
-              pv[kk * 32 + 2 * k + 1] * (__uint_as_float(ud[2 * k + 1]) - dl.y) * p.scale;
-          dk[k] = pack_bf16(d0, d1);
+        for (int k = 0; k < 8; ++k) dz[k] = d4[k];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 dl = dz[k];
+          const float* u = reinterpret_cast<const float*>(ud) + 4 * k;
+          const float* pk = pv + kk * 32 + 4 * k;
+          dk[2 * k] = pack_bf16(pk[0] * (u[0] - dl.x) * p.scale, pk[1] * (u[1] - dl.y) * p.scale);
+          dk[2 * k + 1] =
+              pack_bf16(pk[2] * (u[2] - dl.z) * p.scale, pk[3] * (u[3] - dl.w) * p.scale);
         }
         tmem_st16(tmem_addr(tmem, qd, C_DP + ch * 96 + c * 16), dk);
       }

@@ -41,8 +41,8 @@ constexpr int UNR = 48;
 // Instruction k goes to accumulator (k / run) % n_acc at column acc * n.
 template <int FORM, int BMN, int BG>
 __global__ void __launch_bounds__(128, 1)
-    diag_mma_kernel(int n, int n_acc, int run, int n_blocks, int rnd, unsigned long long* cycles,
-                    int* err) {
+    diag_mma_kernel(int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk,
+                    unsigned long long* cycles, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -50,6 +50,7 @@ __global__ void __launch_bounds__(128, 1)
   __shared__ uint32_t tmem_sh;
   __shared__ volatile int stop;
   __shared__ float sink[4];
+  __shared__ unsigned long long bg_cycles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // operands: small repeating values, or (rnd) values spread like N(0,1)
   // draws (a sum of four uniform hashes), whose bit patterns toggle like
@@ -74,6 +75,7 @@ __global__ void __launch_bounds__(128, 1)
     mbar_init(&bg_bar[1], 1);
     fence_barrier_init();
     stop = 0;
+    bg_cycles = 0;
   }
   if (warp == 0) {
     tmem_alloc(&tmem_sh, 512);
@@ -121,7 +123,7 @@ __global__ void __launch_bounds__(128, 1)
     mma_commit(&bar);
     const bool ok = mbar_wait(&bar, 0, err);
     const unsigned long long t1 = clock64();
-    cycles[blockIdx.x] = ok ? t1 - t0 : 0ull;
+    if (!bg_clk) cycles[blockIdx.x] = ok ? t1 - t0 : 0ull;
     stop = 1;
   } else if (BG == 3 && warp == 1) {
     // background bulk copies until the MMAs are done (bounded)
@@ -141,6 +143,19 @@ __global__ void __launch_bounds__(128, 1)
       for (int k = 0; k < 2; ++k)
         if (issued[k]) mbar_wait(&bg_bar[k], (issued[k] - 1) & 1, err);
     }
+  } else if (BG == 6 && warp > 0) {
+    // background broadcast shared-memory loads (every lane reads the same
+    // 16 bytes), the pattern of per-column softmax statistics
+    const float4* src = reinterpret_cast<const float4*>(sm + BG_OFF + (warp - 1) * 8192);
+    float acc = 0.f;
+    const unsigned long long b0 = clock64();
+    uint32_t nops = 0;
+    for (uint32_t it = 0; it < (1u << 22) && !stop; ++it, ++nops) {
+      const float4 v = src[(it * 7u + (uint32_t)(acc > 1e30f)) & 511];
+      acc += v.x + v.y + v.z + v.w;
+    }
+    if (lane == 0) sink[warp] = acc;
+    if (bg_clk && warp == 1 && lane == 0 && nops > 0) bg_cycles = (clock64() - b0) / nops;
   } else if (BG == 5 && warp > 0) {
     // background exponentials and FMAs, the mix of a softmax, until the
     // MMAs are done
@@ -168,7 +183,9 @@ __global__ void __launch_bounds__(128, 1)
   } else if ((BG == 1 || BG == 2) && warp > 0) {
     // background traffic until the MMAs are done (bounded)
     float acc = 0.f;
-    for (uint32_t it = 0; it < (1u << 22) && !stop; ++it) {
+    const unsigned long long b0 = clock64();
+    uint32_t nops = 0;
+    for (uint32_t it = 0; it < (1u << 22) && !stop; ++it, ++nops) {
       if (BG == 1) {
         uint32_t u[32];
         tmem_ld32(tmem_addr(tmem, warp, BG_TMEM_COL), u);
@@ -181,9 +198,12 @@ __global__ void __launch_bounds__(128, 1)
       }
     }
     if (lane == 0) sink[warp] = acc;
+    // with `bg_clk`, warp 1 reports the mean clocks of one of its operations
+    if (bg_clk && warp == 1 && lane == 0 && nops > 0) bg_cycles = (clock64() - b0) / nops;
   }
   tc_fence_before();
   __syncthreads();
+  if (bg_clk && threadIdx.x == 0) cycles[blockIdx.x] = bg_cycles;
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -191,37 +211,43 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 template <int FORM, int BMN, int BG>
-cudaError_t launch_diag(int n, int n_acc, int run, int n_blocks, int rnd, int n_cta,
+cudaError_t launch_diag(int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk, int n_cta,
                         unsigned long long* cycles, int* err, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(diag_mma_kernel<FORM, BMN, BG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  diag_mma_kernel<FORM, BMN, BG><<<n_cta, 128, SMEM, st>>>(n, n_acc, run, n_blocks, rnd, cycles,
-                                                           err);
+  diag_mma_kernel<FORM, BMN, BG><<<n_cta, 128, SMEM, st>>>(n, n_acc, run, n_blocks, rnd, bg_clk,
+                                                           cycles, err);
   return cudaGetLastError();
 }
 
 template <int FORM, int BMN>
-cudaError_t launch_diag_bg(int bg, int n, int n_acc, int run, int n_blocks, int rnd, int n_cta,
+cudaError_t launch_diag_bg(int bg, int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk,
+                           int n_cta,
                            unsigned long long* cycles, int* err, cudaStream_t st) {
   if (bg == 1)
-    return launch_diag<FORM, BMN, 1>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 1>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
   if (bg == 2)
-    return launch_diag<FORM, BMN, 2>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 2>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
   if (bg == 3)
-    return launch_diag<FORM, BMN, 3>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 3>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
   if (bg == 4)
-    return launch_diag<FORM, BMN, 4>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 4>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
   if (bg == 5)
-    return launch_diag<FORM, BMN, 5>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
-  return launch_diag<FORM, BMN, 0>(n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 5>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+  if (bg == 6)
+    return launch_diag<FORM, BMN, 6>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+  return launch_diag<FORM, BMN, 0>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
 }
 
 template <int FORM>
 cudaError_t launch_diag_form(int bmn, int bg, int n, int n_acc, int run, int n_blocks, int rnd,
-                             int n_cta, unsigned long long* cycles, int* err, cudaStream_t st) {
-  return bmn ? launch_diag_bg<FORM, 1>(bg, n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st)
-             : launch_diag_bg<FORM, 0>(bg, n, n_acc, run, n_blocks, rnd, n_cta, cycles, err, st);
+                             int bg_clk, int n_cta, unsigned long long* cycles, int* err,
+                             cudaStream_t st) {
+  return bmn ? launch_diag_bg<FORM, 1>(bg, n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err,
+                                       st)
+             : launch_diag_bg<FORM, 0>(bg, n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err,
+                                       st);
 }
 
 }  // namespace
@@ -231,7 +257,8 @@ extern "C" laga_status laga_diag_mma_rate(int form, int n, int n_acc, int run, i
                                           int n_cta, unsigned long long* cycles, void* stream) {
   using namespace laga;
   const int op = form & 3, bmn = (form >> 2) & 1, bg = (form >> 3) & 7, rnd = (form >> 6) & 1;
-  if (form < 0 || form >= 128 || bg > 5 || op > 2 || n < 16 || n > 256 || n % 16 != 0 ||
+  const int bg_clk = (form >> 7) & 1;
+  if (form < 0 || form >= 256 || bg > 6 || (bg_clk && bg != 1 && bg != 2 && bg != 6) || op > 2 || n < 16 || n > 256 || n % 16 != 0 ||
       n_acc < 1 || run < 1 || n_instr < 1 || n_instr > (1 << 20) || n_cta < 1 || n_cta > 4096 ||
       !cycles)
     return LAGA_ERR_ARG;
@@ -245,8 +272,8 @@ extern "C" laga_status laga_diag_mma_rate(int form, int n, int n_acc, int run, i
   const int nb = n_instr / UNR;
   int* ew = static_cast<int*>(err);
   cudaError_t e =
-      op == 0   ? launch_diag_form<0>(bmn, bg, n, n_acc, run, nb, rnd, n_cta, cycles, ew, st)
-      : op == 1 ? launch_diag_form<1>(bmn, bg, n, n_acc, run, nb, rnd, n_cta, cycles, ew, st)
-                : launch_diag_form<2>(bmn, bg, n, n_acc, run, nb, rnd, n_cta, cycles, ew, st);
+      op == 0   ? launch_diag_form<0>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, n_cta, cycles, ew, st)
+      : op == 1 ? launch_diag_form<1>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, n_cta, cycles, ew, st)
+                : launch_diag_form<2>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, n_cta, cycles, ew, st);
   return e == cudaSuccess ? LAGA_OK : LAGA_ERR_CUDA;
 }
