@@ -19,7 +19,8 @@
  *
  * Conventions (the page leaves these open; each is the plainest reading):
  *   - d = d_nope + d_rope; causal means key j is visible to query i iff j<=i.
- *   - LayerNorm: biased variance, gain gamma, no bias, eps = ln_eps.
+ *   - LayerNorm: biased variance, gain gamma, no bias, eps = ln_eps (or its
+ *     RMS variant, dims->norm = LAGA_NORM_RMS).
  *   - RoPE rotates pairs (i, i + d_rope/2) by the angle whose cos/sin the
  *     caller passes in cos/sin [S, d_rope/2] (fp32, positions 0..S-1 of the
  *     gathered sequence).  q is passed raw; the library rotates q_rope and
@@ -76,6 +77,12 @@ typedef enum {
  *            memory-trap contrast path, not a performance path. */
 typedef enum { LAGA_FORM_LAGA = 0, LAGA_FORM_EXPLICIT = 1, LAGA_FORM_ABSORBED = 2 } laga_form;
 
+/* Normalisation of the latent (step a1).  The paper's "LN" is LayerNorm:
+ * mean-subtracted, biased variance, gain gamma, no bias.  LAGA_NORM_RMS is
+ * its RMS variant, an extension of the method: no mean subtraction,
+ * L = x * gamma / sqrt(mean(x^2) + eps). */
+typedef enum { LAGA_NORM_LAYER = 0, LAGA_NORM_RMS = 1 } laga_norm;
+
 /* Element type of q, c, W_kv_b, O, dO and dq.  Compute is bf16 operands with
  * fp32 accumulation in both cases; fp32 I/O is rounded to bf16 on-device. */
 typedef enum { LAGA_BF16 = 0, LAGA_FP32 = 1 } laga_dtype;
@@ -95,6 +102,7 @@ typedef struct {
   int causal;       /* must be 1                                               */
   laga_dtype io_dtype;
   laga_form form;
+  laga_norm norm;   /* latent norm of step a1 (LAGA_NORM_LAYER = 0)          */
 } laga_dims;
 
 /* Workspace passes. */
@@ -237,7 +245,7 @@ int laga_last_launch_count(void);
  *   d_kpe_rot   [B, S, n_h_shard, d_rope] fp32: each head's gradient with
  *               respect to the RoPE'd k_pe (summed over heads in head order)
  *   dc          [B, S, d_kv + d_rope] fp32 (output), dgamma [d_kv] fp32 (output)
- * The LayerNorm statistics are recomputed from c.  d_kv above 512 does not
+ * The statistics of the latent norm (dims->norm) are recomputed from c.  d_kv above 512 does not
  * fit the scratch and returns LAGA_ERR_WORKSPACE; other errors as for
  * laga_bwd. */
 laga_status laga_norm_rope_bwd_noalloc(const laga_dims* dims, const void* c, const float* gamma,

@@ -38,6 +38,7 @@ class Workload:
     dtype: str = "bf16"         # I/O dtype of q, c, W_kv_b, O, dq, dO
     seed: int = 1000
     theta: float = 10000.0
+    norm: str = "layer"         # latent norm: "layer" or its RMS variant "rms"
 
     @property
     def d_qk(self):

@@ -18,6 +18,9 @@ Parity status per function (what pins it lives in ``tests/test_oracle.py``):
 
 * ``layernorm``            pinned: torch.nn.functional.layer_norm (fp64),
                            affine-shift invariance, brute-force loops.
+* ``rmsnorm``              pinned: torch.nn.functional.rms_norm (fp64),
+                           positive-scale invariance, not shift-invariant;
+                           its backward by finite differences and autograd.
 * ``rope_tables``/``rope`` pinned: position-0 identity, norm preservation,
                            relative-position shift invariance, brute force.
 * ``forward``              pinned: brute-force Python loops on tiny inputs,
@@ -41,6 +44,10 @@ from .laga import (  # noqa: F401
     Dims,
     layernorm,
     layernorm_backward,
+    rmsnorm,
+    rmsnorm_backward,
+    latent_norm,
+    latent_norm_backward,
     rope_tables,
     rope,
     rope_transpose,

@@ -49,6 +49,7 @@ class Dims:
     head_offset: int = 0
     eps: float = 1e-5
     scale: float | None = None  # None -> 1/sqrt(d_nope + d_rope)
+    norm: str = "layer"         # "layer": the page's LN; "rms": its RMS variant
 
     @property
     def d_qk(self) -> int:
@@ -82,6 +83,42 @@ def layernorm(x, gamma, eps=1e-5):
     rstd = 1.0 / np.sqrt(var + eps)
     xhat = (x - mean[..., None]) * rstd[..., None]
     return xhat * np.asarray(gamma, F64), mean, rstd, xhat
+
+
+def rmsnorm(x, gamma, eps=1e-5):
+    """RMS variant of the latent norm (an extension; the page's norm is LN):
+    no mean subtraction, rstd = 1/sqrt(mean(x^2) + eps).
+
+    Returns (L, mean, rstd, xhat) like ``layernorm``, with mean = 0 and
+    xhat = x * rstd, L = xhat * gamma.
+    """
+    x = np.asarray(x, F64)
+    rstd = 1.0 / np.sqrt((x * x).mean(axis=-1) + eps)
+    xhat = x * rstd[..., None]
+    return xhat * np.asarray(gamma, F64), np.zeros_like(rstd), rstd, xhat
+
+
+def rmsnorm_backward(dL, xhat, rstd, gamma):
+    """Gradient of L = xhat * gamma, xhat = x * rstd, with respect to x and
+    gamma.  With g = dL * gamma and n features:
+    dx = rstd * (g - xhat * mean(g * xhat)),
+    dgamma = sum over all tokens of dL * xhat.
+    """
+    g = dL * np.asarray(gamma, F64)
+    m2 = (g * xhat).mean(axis=-1, keepdims=True)
+    dx = rstd[..., None] * (g - xhat * m2)
+    dgamma = (dL * xhat).reshape(-1, dL.shape[-1]).sum(axis=0)
+    return dx, dgamma
+
+
+def latent_norm(x, gamma, dims):
+    """The latent norm of step a1 that ``dims.norm`` selects."""
+    return (rmsnorm if dims.norm == "rms" else layernorm)(x, gamma, dims.eps)
+
+
+def latent_norm_backward(dL, xhat, rstd, gamma, dims):
+    """Backward of ``latent_norm``."""
+    return (rmsnorm_backward if dims.norm == "rms" else layernorm_backward)(dL, xhat, rstd, gamma)
 
 
 def layernorm_backward(dL, xhat, rstd, gamma):
@@ -157,7 +194,7 @@ def _prologue(q, c, w, gamma, cos, sin, dims: Dims):
     assert q.shape == (B, S, H, dims.d_qk), q.shape
     assert c.shape == (B, S, dims.d_kv + dims.d_rope), c.shape
     x = c[..., :dims.d_kv]
-    L, mean, rstd, xhat = layernorm(x, gamma, dims.eps)
+    L, mean, rstd, xhat = latent_norm(x, gamma, dims)
     kpe_r = rope(c[..., dims.d_kv:], cos, sin)              # [B,S,d_rope]
     q_nope = q[..., :dims.d_nope]                            # [B,S,H,d_nope]
     q_rope_r = rope(q[..., dims.d_nope:], cos, sin)          # [B,S,H,d_rope]
@@ -267,7 +304,7 @@ def backward(saved, dO, block=512):
         out.update(dc=None, dgamma=None, dL=None)
         return out
     dL = np.einsum("bshd,khd->bsk", dKV, saved["W"], optimize=True)
-    dx, dgamma = layernorm_backward(dL, saved["xhat"], saved["rstd"], saved["gamma"])
+    dx, dgamma = latent_norm_backward(dL, saved["xhat"], saved["rstd"], saved["gamma"], dims)
     dkpe_r = dkpe_r_h.sum(axis=2)
     dkpe = rope_transpose(dkpe_r, saved["cos"], saved["sin"])
     out.update(dc=np.concatenate([dx, dkpe], axis=-1), dgamma=dgamma, dL=dL,
@@ -346,7 +383,7 @@ def backward_absorbed(saved, dO, block=512):
     dq = np.concatenate([dq_nope, rope_transpose(dq_rope_r, saved["cos"], saved["sin"])],
                         axis=-1)
     dW = np.concatenate([dWk, dWv], axis=-1).reshape(dims.d_kv, H * dims.d_head_kv)
-    dx, dgamma = layernorm_backward(dLat, saved["xhat"], saved["rstd"], saved["gamma"])
+    dx, dgamma = latent_norm_backward(dLat, saved["xhat"], saved["rstd"], saved["gamma"], dims)
     dkpe = rope_transpose(dkpe_r, saved["cos"], saved["sin"])
     return dict(dq=dq, dc=np.concatenate([dx, dkpe], axis=-1), dw=dW, dgamma=dgamma,
                 dL=dLat, dkpe_r=dkpe_r)

@@ -18,6 +18,7 @@ LAGA_OK, LAGA_ERR_ARG, LAGA_ERR_ALIGN, LAGA_ERR_WORKSPACE = 0, 1, 2, 3
 LAGA_ERR_UNSUPPORTED, LAGA_ERR_CUDA, LAGA_ERR_TIMEOUT = 4, 5, 6
 FORMS = {"laga": 0, "explicit": 1, "absorbed": 2}
 DTYPES = {"bf16": 0, "fp32": 1}
+NORMS = {"layer": 0, "rms": 1}
 WS_SAVED, WS_BWD = 0, 1
 
 EXPORTED = ("laga_workspace_bytes", "laga_workspace_tensor", "laga_fwd", "laga_bwd",
@@ -31,7 +32,8 @@ class LagaDims(ctypes.Structure):
                 ("head_offset", ctypes.c_int), ("n_h_shard", ctypes.c_int),
                 ("d_nope", ctypes.c_int), ("d_rope", ctypes.c_int), ("d_v", ctypes.c_int),
                 ("d_kv", ctypes.c_int), ("scale", ctypes.c_float), ("ln_eps", ctypes.c_float),
-                ("causal", ctypes.c_int), ("io_dtype", ctypes.c_int), ("form", ctypes.c_int)]
+                ("causal", ctypes.c_int), ("io_dtype", ctypes.c_int), ("form", ctypes.c_int),
+                ("norm", ctypes.c_int)]
 
 
 class LagaError(RuntimeError):
@@ -95,10 +97,10 @@ def status_string(status: int) -> str:
 
 def make_dims(S, n_h_shard, *, B=1, n_h_total=None, head_offset=0, d_nope=128, d_rope=64,
               d_v=128, d_kv=512, scale=0.0, ln_eps=1e-5, causal=1, io_dtype="bf16",
-              form="laga") -> LagaDims:
+              form="laga", norm="layer") -> LagaDims:
     return LagaDims(B, S, n_h_shard if n_h_total is None else n_h_total, head_offset, n_h_shard,
                     d_nope, d_rope, d_v, d_kv, scale, ln_eps, causal, DTYPES[io_dtype],
-                    FORMS[form])
+                    FORMS[form], NORMS[norm])
 
 
 def workspace_bytes(dims: LagaDims, pass_: int) -> int:

@@ -33,12 +33,14 @@ class Shard:
     ln_eps: float = 1e-5
     io_dtype: str = "bf16"
     form: str = "laga"
+    norm: str = "layer"      # latent norm: "layer" (LayerNorm) or "rms" (its RMS variant)
 
     def dims(self) -> _lib.LagaDims:
         return _lib.make_dims(self.S, self.H, B=self.B, n_h_total=self.n_h_total,
                               head_offset=self.head_offset, d_nope=self.d_nope,
                               d_rope=self.d_rope, d_v=self.d_v, d_kv=self.d_kv, scale=self.scale,
-                              ln_eps=self.ln_eps, io_dtype=self.io_dtype, form=self.form)
+                              ln_eps=self.ln_eps, io_dtype=self.io_dtype, form=self.form,
+                              norm=self.norm)
 
     @property
     def n_total(self):

@@ -50,15 +50,16 @@ laga_status scratch_on_current_device(float** out) {
   return LAGA_OK;
 }
 
-// One warp per token: recompute the LayerNorm statistics of the latent,
-// dx = rstd (g - mean(g) - xhat mean(g xhat)) with g = dL * gamma, the
+// One warp per token: recompute the norm statistics of the latent,
+// dx = rstd (g - mean(g) - xhat mean(g xhat)) with g = dL * gamma (no
+// mean(g) term for the RMS variant, whose mean is 0), the
 // block's dgamma partial sums, and the k_pe gradient summed over heads in
 // head order and rotated back.
 template <typename T>
 __global__ void __launch_bounds__(256) noalloc_norm_rope_bwd_kernel(
     const T* __restrict__ c, const float* __restrict__ gamma, const float* __restrict__ cosT,
     const float* __restrict__ sinT, const float* __restrict__ dL,
-    const float* __restrict__ dkpe_h, int B, int S, int H, int dr, int dkv, float eps,
+    const float* __restrict__ dkpe_h, int B, int S, int H, int dr, int dkv, float eps, int rms,
     float* __restrict__ dc, float* __restrict__ part) {
   __shared__ float red[kWarps][kCols];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(256) noalloc_norm_rope_bwd_kernel(
       x[i] = col < dkv ? to_f32(crow[col]) : 0.f;
       sum += x[i];
     }
-    const float mu = warp_sum(sum) / dkv;
+    const float mu = rms ? 0.f : warp_sum(sum) / dkv;   // RMS variant: no centring
     float sq = 0.f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -101,7 +102,7 @@ __global__ void __launch_bounds__(256) noalloc_norm_rope_bwd_kernel(
       s1 += g[i];
       s2 += g[i] * xh[i];
     }
-    const float m1 = warp_sum(s1) / dkv, m2 = warp_sum(s2) / dkv;
+    const float m1 = rms ? 0.f : warp_sum(s1) / dkv, m2 = warp_sum(s2) / dkv;
     float* drow = dc + tok * (dkv + dr);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -168,11 +169,11 @@ extern "C" laga_status laga_norm_rope_bwd_noalloc(const laga_dims* dims, const v
   if (p.fp32)
     noalloc_norm_rope_bwd_kernel<float><<<kParts, 256, 0, st>>>(
         static_cast<const float*>(c), gamma, cos, sin, d_latent, d_kpe_rot, p.B, p.S, p.H, p.dr,
-        p.dkv, p.d.ln_eps, dc, part);
+        p.dkv, p.d.ln_eps, (int)p.rms, dc, part);
   else
     noalloc_norm_rope_bwd_kernel<__nv_bfloat16><<<kParts, 256, 0, st>>>(
         static_cast<const __nv_bfloat16*>(c), gamma, cos, sin, d_latent, d_kpe_rot, p.B, p.S, p.H,
-        p.dr, p.dkv, p.d.ln_eps, dc, part);
+        p.dr, p.dkv, p.d.ln_eps, (int)p.rms, dc, part);
   if (cudaGetLastError() != cudaSuccess) return LAGA_ERR_CUDA;
   noalloc_dgamma_reduce_kernel<<<(p.dkv + 127) / 128, 128, 0, st>>>(part, p.dkv, dgamma);
   return cudaGetLastError() == cudaSuccess ? LAGA_OK : LAGA_ERR_CUDA;

@@ -49,6 +49,7 @@ struct Plan {
   int B = 0, S = 0, H = 0, dn = 0, dr = 0, dv = 0, dkv = 0;
   bool canonical = false;   // dims are 128/64/128/512 and I/O is bf16
   bool fp32 = false;
+  bool rms = false;         // RMS variant of the latent norm (no mean subtraction)
   float scale = 0.f;
   size_t off[N_BUF] = {};
   size_t len[N_BUF] = {};
@@ -103,6 +104,7 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
   if (d.io_dtype != LAGA_BF16 && d.io_dtype != LAGA_FP32) return LAGA_ERR_ARG;
   if (d.form != LAGA_FORM_LAGA && d.form != LAGA_FORM_EXPLICIT && d.form != LAGA_FORM_ABSORBED)
     return LAGA_ERR_ARG;
+  if (d.norm != LAGA_NORM_LAYER && d.norm != LAGA_NORM_RMS) return LAGA_ERR_ARG;
   if (d.causal != 1) return LAGA_ERR_UNSUPPORTED;
   // Keep every element index inside 32-bit row counts times 64-bit strides.
   if ((long long)d.B * d.S * d.n_h_shard > (1LL << 31) - 1) return LAGA_ERR_ARG;
@@ -111,6 +113,7 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
   p->B = d.B; p->S = d.S; p->H = d.n_h_shard;
   p->dn = d.d_nope; p->dr = d.d_rope; p->dv = d.d_v; p->dkv = d.d_kv;
   p->fp32 = d.io_dtype == LAGA_FP32;
+  p->rms = d.norm == LAGA_NORM_RMS;
   p->canonical = !p->fp32 && d.d_nope == 128 && d.d_rope == 64 && d.d_v == 128 && d.d_kv == 512;
   p->scale = d.scale > 0.f ? d.scale : 1.0f / sqrtf((float)(d.d_nope + d.d_rope));
 

@@ -40,7 +40,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) prep_fwd_kernel(
     const T* __restrict__ q, const T* __restrict__ c, const float* __restrict__ gamma,
     const float* __restrict__ cosT, const float* __restrict__ sinT, int B, int S, int H, int dn,
-    int dr, int dkv, float eps, __nv_bfloat16* __restrict__ L, float* __restrict__ mean_o,
+    int dr, int dkv, float eps, int rms, __nv_bfloat16* __restrict__ L, float* __restrict__ mean_o,
     float* __restrict__ rstd_o, __nv_bfloat16* __restrict__ kpe, __nv_bfloat16* __restrict__ qr,
     __nv_bfloat16* __restrict__ qn_pad) {
   const int lane = threadIdx.x & 31;
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) prep_fwd_kernel(
     x[i] = col < dkv ? to_f32(crow[col]) : 0.f;
     sum += x[i];
   }
-  const float mu = warp_sum(sum) / dkv;
+  const float mu = rms ? 0.f : warp_sum(sum) / dkv;   // RMS variant: no centring
   float sq = 0.f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(
     const float* __restrict__ dL, const T* __restrict__ c, const float* __restrict__ mean,
     const float* __restrict__ rstd, const float* __restrict__ gamma,
     const float* __restrict__ dkpe_h, const float* __restrict__ cosT,
-    const float* __restrict__ sinT, int B, int S, int H, int dr, int dkv,
+    const float* __restrict__ sinT, int B, int S, int H, int dr, int dkv, int rms,
     float* __restrict__ dc, float* __restrict__ dg_part) {
   __shared__ float red[WARPS][512];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(256) norm_bwd_kernel(
       s1 += g[i];
       s2 += g[i] * xh[i];
     }
-    const float m1 = warp_sum(s1) / dkv, m2 = warp_sum(s2) / dkv;
+    // the RMS variant has no centring, so no mean(g) term
+    const float m1 = rms ? 0.f : warp_sum(s1) / dkv, m2 = warp_sum(s2) / dkv;
     float* drow = dc + tok * (dkv + dr);
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -335,7 +336,7 @@ LAGA_DEVINL void rope_chunk_pair(const __nv_bfloat16* src, __nv_bfloat16* dst, i
 __global__ void __launch_bounds__(256) prep_fwd_v_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ c,
     const float* __restrict__ gamma, const float* __restrict__ cosT,
-    const float* __restrict__ sinT, int S, int H, long long tokens, float eps,
+    const float* __restrict__ sinT, int S, int H, long long tokens, float eps, int rms,
     __nv_bfloat16* __restrict__ L, float* __restrict__ mean_o, float* __restrict__ rstd_o,
     __nv_bfloat16* __restrict__ kpe, __nv_bfloat16* __restrict__ qr) {
   const int lane = threadIdx.x & 31;
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(256) prep_fwd_v_kernel(
   float sum = 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) sum += x[0][k] + x[1][k];
-  const float mu = warp_sum(sum) * (1.0f / 512);
+  const float mu = rms ? 0.f : warp_sum(sum) * (1.0f / 512);   // RMS variant: no centring
   float sq = 0.f;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -477,7 +478,7 @@ __global__ void __launch_bounds__(256) norm_bwd_v_kernel(
     const float* __restrict__ mean, const float* __restrict__ rstd,
     const float* __restrict__ gamma, const float* __restrict__ dkpe_h,
     const float* __restrict__ cosT, const float* __restrict__ sinT, int S, int H,
-    long long tokens, float* __restrict__ dc, float* __restrict__ dg_part) {
+    long long tokens, int rms, float* __restrict__ dc, float* __restrict__ dg_part) {
   __shared__ float red[WARPS][512];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   float gm[2][8], dg[2][8];
@@ -522,7 +523,8 @@ __global__ void __launch_bounds__(256) norm_bwd_v_kernel(
         s2 += g[hh][k] * xh[hh][k];
       }
     }
-    const float m1 = warp_sum(s1) * (1.0f / 512), m2 = warp_sum(s2) * (1.0f / 512);
+    // the RMS variant has no centring, so no mean(g) term
+    const float m1 = rms ? 0.f : warp_sum(s1) * (1.0f / 512), m2 = warp_sum(s2) * (1.0f / 512);
     float* drow = dc + tok * 576;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -615,15 +617,15 @@ cudaError_t launch_prep_fwd(const Plan& p, const Ptrs& x, cudaStream_t st) {
   if (p.canonical)
     prep_fwd_v_kernel<<<g, 256, 0, st>>>((const __nv_bfloat16*)x.q, (const __nv_bfloat16*)x.c,
                                          x.gamma, x.cos, x.sin, p.S, p.H, p.tokens(), p.d.ln_eps,
-                                         L, mean, rstd, kpe, qr);
+                                         (int)p.rms, L, mean, rstd, kpe, qr);
   else if (p.fp32)
     prep_fwd_kernel<float><<<g, 256, 0, st>>>((const float*)x.q, (const float*)x.c, x.gamma, x.cos,
                                               x.sin, p.B, p.S, p.H, p.dn, p.dr, p.dkv, p.d.ln_eps,
-                                              L, mean, rstd, kpe, qr, qn);
+                                              (int)p.rms, L, mean, rstd, kpe, qr, qn);
   else
     prep_fwd_kernel<__nv_bfloat16><<<g, 256, 0, st>>>(
         (const __nv_bfloat16*)x.q, (const __nv_bfloat16*)x.c, x.gamma, x.cos, x.sin, p.B, p.S, p.H,
-        p.dn, p.dr, p.dkv, p.d.ln_eps, L, mean, rstd, kpe, qr, qn);
+        p.dn, p.dr, p.dkv, p.d.ln_eps, (int)p.rms, L, mean, rstd, kpe, qr, qn);
   return cudaGetLastError();
 }
 
@@ -684,15 +686,15 @@ cudaError_t launch_norm_bwd(const Plan& p, const Ptrs& x, const float* dL, cudaS
   if (p.canonical)
     norm_bwd_v_kernel<<<NGP, 256, 0, st>>>(dL, (const __nv_bfloat16*)x.c, x.buf<float>(p, W_MEAN),
                                            x.buf<float>(p, W_RSTD), x.gamma, dk, x.cos, x.sin, p.S,
-                                           p.H, p.tokens(), x.dc, part);
+                                           p.H, p.tokens(), (int)p.rms, x.dc, part);
   else if (p.fp32)
     norm_bwd_kernel<float><<<NGP, 256, 0, st>>>(dL, (const float*)x.c, x.buf<float>(p, W_MEAN),
                                                 x.buf<float>(p, W_RSTD), x.gamma, dk, x.cos, x.sin,
-                                                p.B, p.S, p.H, p.dr, p.dkv, x.dc, part);
+                                                p.B, p.S, p.H, p.dr, p.dkv, (int)p.rms, x.dc, part);
   else
     norm_bwd_kernel<__nv_bfloat16><<<NGP, 256, 0, st>>>(
         dL, (const __nv_bfloat16*)x.c, x.buf<float>(p, W_MEAN), x.buf<float>(p, W_RSTD), x.gamma,
-        dk, x.cos, x.sin, p.B, p.S, p.H, p.dr, p.dkv, x.dc, part);
+        dk, x.cos, x.sin, p.B, p.S, p.H, p.dr, p.dkv, (int)p.rms, x.dc, part);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;

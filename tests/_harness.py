@@ -32,7 +32,7 @@ def shard_of(wl: Workload, form="laga", **over):
     import sequence_latent_norm_gb300 as pkg
     kw = dict(S=wl.S, H=wl.H, n_h_total=wl.n_h_total, head_offset=wl.head_offset, B=wl.B,
               d_nope=wl.d_nope, d_rope=wl.d_rope, d_v=wl.d_v, d_kv=wl.d_kv,
-              io_dtype=wl.dtype, form=form)
+              io_dtype=wl.dtype, form=form, norm=wl.norm)
     kw.update(over)
     return pkg.Shard(**kw)
 
@@ -64,7 +64,8 @@ def gpu_run(wl: Workload, cpu=None, form="laga", device="cuda:0", heads=None):
 
 def oracle_dims(wl: Workload):
     return oracle.Dims(S=wl.S, H=wl.H, d_nope=wl.d_nope, d_rope=wl.d_rope, d_v=wl.d_v,
-                       d_kv=wl.d_kv, B=wl.B, n_h_total=wl.n_h_total, head_offset=wl.head_offset)
+                       d_kv=wl.d_kv, B=wl.B, n_h_total=wl.n_h_total, head_offset=wl.head_offset,
+                       norm=wl.norm)
 
 
 def _bf16(x):

@@ -118,3 +118,13 @@ def test_noalloc_rejects_latent_wider_than_its_scratch(lib):
                                        null, null, null)
     assert st == lib.LAGA_ERR_WORKSPACE
     assert "workspace" in lib.status_string(st)
+
+
+def test_latent_norm_field_is_validated(lib):
+    """dims.norm selects the latent norm (0 LayerNorm, 1 its RMS variant);
+    any other value is refused by the plan, before any launch."""
+    assert lib.workspace_bytes(lib.make_dims(256, 2, norm="rms"), lib.WS_SAVED) == \
+        lib.workspace_bytes(lib.make_dims(256, 2), lib.WS_SAVED)
+    d = lib.make_dims(256, 2)
+    d.norm = 2
+    assert lib.workspace_bytes(d, lib.WS_SAVED) == 0

@@ -145,6 +145,25 @@ def test_layernorm_matches_torch_and_is_affine_invariant():
     np.testing.assert_allclose(L2, L3, atol=1e-12)
 
 
+def test_rmsnorm_matches_torch_and_is_scale_but_not_shift_invariant():
+    """The RMS variant of the latent norm: torch's rms_norm; invariant to a
+    positive scale of x (eps = 0), but, having no centring, not to a shift
+    (a LayerNorm by mistake would be)."""
+    rng = np.random.default_rng(40)
+    x = rng.standard_normal((3, 7, 16))
+    g = 1.0 + 0.1 * rng.standard_normal(16)
+    L, mean, rstd, xhat = orc.rmsnorm(x, g, 1e-5)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (16,), weight=torch.from_numpy(g),
+                                       eps=1e-5).numpy()
+    np.testing.assert_allclose(L, ref, atol=1e-13)
+    assert np.all(mean == 0.0)
+    L2, _, _, _ = orc.rmsnorm(3.5 * x, g, 0.0)
+    L3, _, _, _ = orc.rmsnorm(x, g, 0.0)
+    np.testing.assert_allclose(L2, L3, atol=1e-12)
+    L4, _, _, _ = orc.rmsnorm(x + 2.0, g, 0.0)
+    assert np.abs(L4 - L3).max() > 0.1
+
+
 # ----------------------------------------------------------------- closed forms
 def test_zero_query_gives_running_mean_and_log_count():
     rng = np.random.default_rng(5)
@@ -186,10 +205,12 @@ def test_lse_normalises_every_row():
 
 
 # ----------------------------------------------------------------- library reduction
-def test_no_rope_case_reduces_to_torch_sdpa_forward_and_autograd():
-    """d_rope = 0: the method is causal SDPA over (q, LN(x) W^k, LN(x) W^v)."""
+@pytest.mark.parametrize("norm", ["layer", "rms"])
+def test_no_rope_case_reduces_to_torch_sdpa_forward_and_autograd(norm):
+    """d_rope = 0: the method is causal SDPA over (q, N(x) W^k, N(x) W^v),
+    N = LayerNorm or its RMS variant."""
     rng = np.random.default_rng(8)
-    d = Dims(S=11, H=2, d_nope=8, d_rope=0, d_v=6, d_kv=10)
+    d = Dims(S=11, H=2, d_nope=8, d_rope=0, d_v=6, d_kv=10, norm=norm)
     q, c, w, gamma, cos, sin, dO = _rand_problem(rng, d)
     O, LSE, st = orc.forward(q, c, w, gamma, cos, sin, d)
     g = orc.backward(st, dO)
@@ -198,7 +219,10 @@ def test_no_rope_case_reduces_to_torch_sdpa_forward_and_autograd():
     tc = torch.tensor(c, requires_grad=True)
     tw = torch.tensor(w, requires_grad=True)
     tg = torch.tensor(gamma, requires_grad=True)
-    L = torch.nn.functional.layer_norm(tc, (d.d_kv,), weight=tg, bias=None, eps=d.eps)
+    if norm == "rms":
+        L = torch.nn.functional.rms_norm(tc, (d.d_kv,), weight=tg, eps=d.eps)
+    else:
+        L = torch.nn.functional.layer_norm(tc, (d.d_kv,), weight=tg, bias=None, eps=d.eps)
     kv = (L @ tw).view(1, d.S, d.H, d.d_head_kv)
     k, v = kv[..., :d.d_nope], kv[..., d.d_nope:]
     o = torch.nn.functional.scaled_dot_product_attention(
@@ -224,12 +248,14 @@ def _loss(q, c, w, gamma, cos, sin, dO, dims):
     return float((O * dO).sum())
 
 
+@pytest.mark.parametrize("norm", ["layer", "rms"])
 @pytest.mark.parametrize("name", ["q", "c", "w", "gamma"])
-def test_backward_matches_central_differences(name):
+def test_backward_matches_central_differences(name, norm):
     rng = np.random.default_rng(9)
-    q, c, w, gamma, cos, sin, dO = _rand_problem(rng, FD)
+    FD_ = dataclasses.replace(FD, norm=norm)
+    q, c, w, gamma, cos, sin, dO = _rand_problem(rng, FD_)
     args = dict(q=q, c=c, w=w, gamma=gamma)
-    _, _, st = orc.forward(q, c, w, gamma, cos, sin, FD)
+    _, _, st = orc.forward(q, c, w, gamma, cos, sin, FD_)
     g = orc.backward(st, dO)
     analytic = {"q": g["dq"], "c": g["dc"], "gamma": g["dgamma"]}
     if name == "w":
@@ -243,9 +269,9 @@ def test_backward_matches_central_differences(name):
     for idx in np.ndindex(x.shape):
         old = x[idx]
         x[idx] = old + h
-        fp = _loss(dO=dO, cos=cos, sin=sin, dims=FD, **args)
+        fp = _loss(dO=dO, cos=cos, sin=sin, dims=FD_, **args)
         x[idx] = old - h
-        fm = _loss(dO=dO, cos=cos, sin=sin, dims=FD, **args)
+        fm = _loss(dO=dO, cos=cos, sin=sin, dims=FD_, **args)
         x[idx] = old
         num[idx] = (fp - fm) / (2 * h)
     err = np.linalg.norm(analytic[name] - num) / max(np.linalg.norm(num), 1e-30)

@@ -176,3 +176,20 @@ def test_bwd_overlap_entry_point_is_bitwise_equal_to_laga_bwd():
         pkg._lib.sync_check()
         for x, y in zip(a, b):
             assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("wl,form", [
+    (config(1, S=333, H=3, B=2, n_h_total=7, head_offset=2, norm="rms"), "laga"),
+    (config(1, S=1000, H=4, norm="rms"), "laga"),
+    (config(1, S=200, H=2, norm="rms"), "absorbed"),
+    (config(0, norm="rms"), "laga"),
+    (config(1, S=150, H=3, d_kv=256, norm="rms"), "laga"),
+], ids=["ragged-B2", "S1000", "absorbed", "tiny-fp32", "dkv256"])
+def test_rms_latent_norm_variant_matches_oracle(wl, form):
+    """The RMS variant of the latent norm (no centring) through the whole
+    path: forward, dq, dc, dW and dgamma against the oracle's rmsnorm."""
+    cpu = make_inputs(wl)
+    got = gpu_run(wl, cpu, form=form)
+    ref = oracle_run(wl, cpu)
+    check_forward(got, ref, f"rms {wl.name} S={wl.S}", form=form)
+    check_grads(got, ref, where=f"rms {wl.name} S={wl.S}")

@@ -5,8 +5,9 @@ whole device for its own pool, an embedding that owns only the tensors it
 passes in) use laga_norm_rope_bwd_noalloc, which keeps its scratch in a
 fixed array inside the library.  This test calls it through the C ABI on two
 calls in a row of different sizes (the shared scratch keeps the previous
-call's contents) and checks dc and dgamma against the fp64 oracle's
-LayerNorm backward and RoPE transpose of the same upstream gradients, and
+call's contents; the second uses the RMS variant of the latent norm) and
+checks dc and dgamma against the fp64 oracle's norm backward and RoPE
+transpose of the same upstream gradients, and
 against what laga_bwd produced from them (only the recomputed LayerNorm
 statistics differ, so the two agree to fp32 rounding).  The file name sorts
 last so a run that stops at the first failure has already run every other
@@ -40,8 +41,9 @@ def _oracle_norm_rope_bwd(cpu, wl, d_latent, d_kpe):
     """dc = [LayerNorm backward of d_latent | RoPE transpose of sum_h d_kpe]
     and dgamma, from the oracle in fp64."""
     c = as_f64(cpu["c"]).reshape(wl.B * wl.S, -1)
-    _, _, rstd, xhat = oracle.layernorm(c[:, :wl.d_kv], as_f64(cpu["gamma"]))
-    dx, dg = oracle.layernorm_backward(as_f64(d_latent), xhat, rstd, as_f64(cpu["gamma"]))
+    d = oracle.Dims(S=wl.S, H=wl.H, norm=wl.norm)
+    _, _, rstd, xhat = oracle.latent_norm(c[:, :wl.d_kv], as_f64(cpu["gamma"]), d)
+    dx, dg = oracle.latent_norm_backward(as_f64(d_latent), xhat, rstd, as_f64(cpu["gamma"]), d)
     dk = as_f64(d_kpe).sum(axis=1).reshape(wl.B, wl.S, wl.d_rope)
     dkpe = oracle.rope_transpose(dk, as_f64(cpu["cos"]), as_f64(cpu["sin"]))
     dc = np.concatenate([dx.reshape(wl.B, wl.S, wl.d_kv), dkpe], axis=-1)
@@ -52,7 +54,7 @@ def test_noalloc_norm_rope_bwd_matches_oracle_on_two_calls():
     import sequence_latent_norm_gb300 as pkg
     lib = pkg._lib
     dev = torch.device("cuda:0")
-    for wl in (config(1, S=1000, H=4), config(1, S=300, H=2, seed=77, B=2)):
+    for wl in (config(1, S=1000, H=4), config(1, S=300, H=2, seed=77, B=2, norm="rms")):
         cpu = make_inputs(wl)
         t = {k: v.to(dev) for k, v in cpu.items()}
         run = pkg.Laga(shard_of(wl), device=dev)
@@ -76,6 +78,7 @@ def test_noalloc_norm_rope_bwd_matches_oracle_on_two_calls():
             g, r = as_f64(got), as_f64(ref)
             assert np.isfinite(g).all(), name
             e_or, e_self = rel_fro(g, orc), rel_fro(g, r)
-            print(f"S={wl.S} B={wl.B} {name}: rel-fro vs oracle {e_or:.2e}, vs laga_bwd {e_self:.2e}")
+            print(f"S={wl.S} B={wl.B} {wl.norm} {name}: rel-fro vs oracle {e_or:.2e}, "
+                  f"vs laga_bwd {e_self:.2e}")
             assert e_or <= NOALLOC_REL_FRO, f"{name} rel-fro vs oracle {e_or:.3e}"
             assert e_self <= NOALLOC_REL_FRO, f"{name} rel-fro vs laga_bwd {e_self:.3e}"
