@@ -575,6 +575,10 @@ def run_mma_rates():
             print(json.dumps({"smem_broadcast_load_latency": {
                 "clk_per_load": float(c.median()),
                 "alongside": f"{forms[op]} N={n} MMAs x {instr}"}}), flush=True)
+    # one issuing thread against two (lane 0 of two warps, own accumulators)
+    for n in (64, 128):
+        for op in (0, 1):
+            cases.append((op | 4 | 64 | 256, n, 1, 1))
     for form, n, n_acc, run in cases:
         for rep in range(2):           # the first launch warms clocks and caches
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -593,6 +597,7 @@ def run_mma_rates():
                                        "b_major": "MN" if form & 4 else "K",
                                        "background": bgs[(form >> 3) & 7],
                                        "operands": "N(0,1)-like" if form & 64 else "small",
+                                       "issuers": 2 if form & 256 else 1,
                                        "N": n,
                                        "accumulators": n_acc,
                                        "run": run, "clk_per_mma": round(clk, 1),

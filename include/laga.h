@@ -194,7 +194,8 @@ laga_status laga_selftest_wait_timeout(void* stream);
  *   form   bits 0-1  0: A and B in shared memory; 1: A in TMEM, B in shared
  *                    memory; 2: the two alternating
  *          bit 2     B MN-major (64-wide N boxes) instead of K-major
- *          bits 3-5  while the MMAs run, the CTA's other three warps
+ *          bits 3-5  while the MMAs run, the CTA's other seven warps (one on
+ *                    the issuing thread's SM sub-partition)
  *                    0: idle; 1: stream TMEM loads from other columns;
  *                    2: stream 16-byte shared-memory stores;
  *                    3: stream 16 KB bulk copies (TMA) into shared memory;

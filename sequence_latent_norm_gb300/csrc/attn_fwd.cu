@@ -2,7 +2,7 @@
 // (Algorithm 1 step 5: scores = (q_nope||q_rope)(k_nope||k_pe)^T / sqrt(d),
 // out = softmax(scores) v; Section 5.3: k_pe shared by all heads).
 //
-// One CTA per (128-row query tile, head, batch), 11 warps:
+// One CTA per (128-row query tile, head, batch), 12 warps:
 //   warps 0-7  softmax: warp w owns query rows 32*(w%4) .. +32 (TMEM lanes)
 //              and key-column half w/4 of every score tile.  A thread reads
 //              its 64 scores of S_j from TMEM, applies the causal mask on
@@ -17,15 +17,22 @@
 //   warp 8     TMA producer of Q once (q_nope | RoPE'd q_rope, 3 boxes) and
 //              per key tile K_j (k_nope | k_pe, 3 boxes) into a two-stage
 //              ring; warp 10 the same for V_j (2 boxes).
-//   warp 9     TMEM allocator and MMA issuer: S_{j+1} = Q K_{j+1}^T (12
-//              K-steps) is issued before O += P_j V_j (8 K-steps, P from
-//              TMEM), so the tensor core works on the next tile while the
-//              softmax warps handle this one.
+//   warp 9     TMEM allocator and issuer of the score MMAs: S_j = Q K_j^T
+//              (12 K-steps) into S buffer j%3, once P_{j-3} V_{j-3} has
+//              consumed that buffer, so the tensor core works on the next
+//              tile while the softmax warps handle this one.
+//   warp 11    issuer of O += P_j V_j (8 K-steps, P from TMEM) once the
+//              softmax warps have written P_j.  One thread can issue a
+//              tcgen05.mma only every ~50 clocks, close to the 64 clocks an
+//              N=128 MMA takes, and every barrier wait on the issuing
+//              thread would leave the tensor core idle; two issuers keep
+//              it fed while each waits on its own barriers.
 // Epilogue: the rows of O, divided by l, are staged as bf16 in the idle Q tile (two 128 x 64
 // swizzled boxes) and written by TMA stores after the final barrier.
-// TMEM columns: S/P double buffer [0,256) (P of key columns 0-63 packed into
+// TMEM columns: S/P triple buffer [0,384) (P of key columns 0-63 packed into
 // the first 32 columns of a buffer, of 64-127 into columns 64-95), O
-// [256,384).
+// [384,512).  With three buffers, S_{j+2} can be issued while P_j V_j is
+// still pending, so the score MMAs of later tiles run during softmax j.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -42,11 +49,12 @@ constexpr int Q_BYTES = 3 * BOX;
 constexpr int K_BYTES = 3 * BOX;
 constexpr int V_BYTES = 2 * BOX;
 constexpr int SMEM_BYTES = Q_BYTES + 2 * (K_BYTES + V_BYTES) + 1024;
-constexpr int THREADS = 352;
+constexpr int THREADS = 384;
 constexpr int N_SOFTMAX = 8;
-constexpr int W_PROD = 8, W_MMA = 9, W_VPROD = 10;
+constexpr int W_PROD = 8, W_MMA = 9, W_VPROD = 10, W_PV = 11;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int O_COL = 256;
+constexpr int NSB = 3;                  // S/P buffers in TMEM
+constexpr int O_COL = NSB * BN;         // 384
 constexpr float RESCALE_LOG2 = 8.0f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -70,14 +78,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* Qs = sm;
   uint8_t* Ks = sm + Q_BYTES;
   uint8_t* Vs = Ks + 2 * K_BYTES;
-  // bar_s[st]: S_j in TMEM, which also means K stage st has been read;
-  // bar_ve[st]: P_j V_j done, so V stage st and S buffer st are free and O
-  // holds every product up to tile j
-  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_ve[2], bar_s[2], bar_p[2];
+  // Per S buffer b = j % 3 (phase parity (j / 3) & 1): bar_s[b], S_j in
+  // TMEM (so K stage j % 2 has been read); bar_p[b], P_j written; bar_ve[b],
+  // P_j V_j done (so S buffer b and V stage j % 2 are free, and O holds
+  // every product up to tile j).  Per K/V ring stage j % 2: bar_kf, bar_vf.
+  __shared__ uint64_t bar_q, bar_kf[2], bar_vf[2], bar_ve[NSB], bar_s[NSB], bar_p[NSB];
   // row-max exchange between the two warps of a query-row quadrant, per S
   // buffer; the final row-sum exchange
-  __shared__ uint64_t bar_mx[4][2], bar_lx[4];
-  __shared__ float red_mx[2][2][BM], red_l[2][BM];
+  __shared__ uint64_t bar_mx[4][NSB], bar_lx[4];
+  __shared__ float red_mx[NSB][2][BM], red_l[2][BM];
   __shared__ uint32_t tmem_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -93,13 +102,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bar_kf[i], 1);
       mbar_init(&bar_vf[i], 1);
+    }
+    for (int i = 0; i < NSB; ++i) {
       mbar_init(&bar_ve[i], 1);
       mbar_init(&bar_s[i], 1);
       mbar_init(&bar_p[i], N_SOFTMAX);
     }
     for (int q = 0; q < 4; ++q) {
-      mbar_init(&bar_mx[q][0], 2);
-      mbar_init(&bar_mx[q][1], 2);
+      for (int i = 0; i < NSB; ++i) mbar_init(&bar_mx[q][i], 2);
       mbar_init(&bar_lx[q], 2);
     }
     fence_barrier_init();
@@ -126,7 +136,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int j = 0; j < n_kt; ++j) {
         const int st = j & 1;
         const int k0 = j * BN;
-        if (j >= 2 && !mbar_wait(&bar_s[st], ((j >> 1) - 1) & 1, p.err)) break;
+        // stage st is free once S_{j-2} is done
+        if (j >= 2 && !mbar_wait(&bar_s[(j - 2) % NSB], ((j - 2) / NSB) & 1, p.err)) break;
         uint8_t* kd = Ks + st * K_BYTES;
         mbar_arrive_expect_tx(&bar_kf[st], K_BYTES);
         tma_load_4d(kd, &tm.kv, &bar_kf[st], 0, k0, h, b);
@@ -140,7 +151,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       for (int j = 0; j < n_kt; ++j) {
         const int st = j & 1;
-        if (j >= 2 && !mbar_wait(&bar_ve[st], ((j >> 1) - 1) & 1, p.err)) break;
+        // stage st is free once P_{j-2} V_{j-2} is done
+        if (j >= 2 && !mbar_wait(&bar_ve[(j - 2) % NSB], ((j - 2) / NSB) & 1, p.err)) break;
         uint8_t* vd = Vs + st * V_BYTES;
         mbar_arrive_expect_tx(&bar_vf[st], V_BYTES);
         tma_load_4d(vd, &tm.kv, &bar_vf[st], 128, j * BN, h, b);
@@ -148,41 +160,43 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp == W_MMA) {
+    // score MMAs: S_j into buffer j%3 once K_j has landed and P_{j-3} V_{j-3}
+    // (issued by warp W_PV) has read the buffer
     if (lane == 0) {
       const uint32_t idS = idesc_bf16(BM, BN, 0, 0);
-      const uint32_t idO = idesc_bf16(BM, 128, 0, 1);
-      const uint32_t qa = smem_u32(Qs);
-      const uint32_t qlo = sdesc_lo(qa, 16);
+      const uint32_t qlo = sdesc_lo(smem_u32(Qs), 16);
       bool ok = mbar_wait(&bar_q, 0, p.err);
-      auto issue_s = [&](int j) -> bool {
-        const int st = j & 1;
-        if (!mbar_wait(&bar_kf[st], (j >> 1) & 1, p.err)) return false;
+      for (int j = 0; ok && j < n_kt; ++j) {
+        const int sb = j % NSB, st = j & 1;
+        if (j >= NSB && !mbar_wait(&bar_ve[sb], ((j - NSB) / NSB) & 1, p.err)) break;
+        if (!mbar_wait(&bar_kf[st], (j >> 1) & 1, p.err)) break;
         tc_fence_after();
         const uint32_t klo = sdesc_lo(smem_u32(Ks + st * K_BYTES), 16);
-        const uint32_t d = tmem + st * BN;
+        const uint32_t d = tmem + sb * BN;
 #pragma unroll
         for (int s = 0; s < 12; ++s) {
           const uint32_t off = ((s >> 2) * BOX + (s & 3) * 32) >> 4;
           mma_ss(d, sdesc_make(qlo + off), sdesc_make(klo + off), idS, s > 0);
         }
-        mma_commit(&bar_s[st]);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kt; ++j) {
-        if (j + 1 < n_kt && !issue_s(j + 1)) break;
-        const int st = j & 1;
-        if (!mbar_wait(&bar_p[st], (j >> 1) & 1, p.err)) break;
+        mma_commit(&bar_s[sb]);
+      }
+    }
+  } else if (warp == W_PV) {
+    // O += P_j V_j once the softmax warps have written P_j and V_j has landed
+    if (lane == 0) {
+      const uint32_t idO = idesc_bf16(BM, 128, 0, 1);
+      for (int j = 0; j < n_kt; ++j) {
+        const int sb = j % NSB, st = j & 1;
+        if (!mbar_wait(&bar_p[sb], (j / NSB) & 1, p.err)) break;
         if (!mbar_wait(&bar_vf[st], (j >> 1) & 1, p.err)) break;
         tc_fence_after();
         const uint32_t vlo = sdesc_lo(smem_u32(Vs + st * V_BYTES), BOX);
-        const uint32_t pa = tmem + st * BN;
+        const uint32_t pa = tmem + sb * BN;
 #pragma unroll
         for (int s = 0; s < 8; ++s)
           mma_ts(tmem + O_COL, pa + (s < 4 ? 8 * s : 64 + 8 * (s - 4)),
-                 sdesc_make(vlo + s * (2048 >> 4)), idO,
-                 (j > 0 || s > 0) ? 1u : 0u);
-        mma_commit(&bar_ve[st]);
+                 sdesc_make(vlo + s * (2048 >> 4)), idO, (j > 0 || s > 0) ? 1u : 0u);
+        mma_commit(&bar_ve[sb]);
       }
     }
   } else {
@@ -194,8 +208,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     float m = -INFINITY, l = 0.f;       // l: this half's part of the row sum
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
-      const int st = j & 1;
-      if (!mbar_wait(&bar_s[st], (j >> 1) & 1, p.err)) { ok = false; break; }
+      const int st = j % NSB;   // S buffer
+      if (!mbar_wait(&bar_s[st], (j / NSB) & 1, p.err)) { ok = false; break; }
       tc_fence_after();
       float s[64];
       {
@@ -217,14 +231,14 @@ __global__ void __launch_bounds__(THREADS, 1)
       red_mx[st][ch][r] = mx;
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_mx[qd][st]);
-      if (!mbar_wait(&bar_mx[qd][st], (j >> 1) & 1, p.err)) { ok = false; break; }
+      if (!mbar_wait(&bar_mx[qd][st], (j / NSB) & 1, p.err)) { ok = false; break; }
       mx = fmaxf(mx, red_mx[st][ch ^ 1][r]) * p.sl2;
       const float m_new = (mx > m + RESCALE_LOG2) ? mx : m;
       const float alpha = ex2(m - m_new);
       const bool need = j > 0 && m_new != m;
       if (__any_sync(0xffffffffu, need)) {
         // O must hold P_{j-1} V_{j-1} before it is rescaled in place.
-        if (!mbar_wait(&bar_ve[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err)) { ok = false; break; }
+        if (!mbar_wait(&bar_ve[(j - 1) % NSB], ((j - 1) / NSB) & 1, p.err)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -266,8 +280,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     // ---------------------------------------------------------- epilogue
     // O is complete once P V of the last tile is done (each stage barrier
     // is waited for its own latest phase, so the parity test is exact)
-    if (ok && n_kt >= 2) ok = mbar_wait(&bar_ve[(n_kt - 2) & 1], ((n_kt - 2) >> 1) & 1, p.err);
-    if (ok) ok = mbar_wait(&bar_ve[(n_kt - 1) & 1], ((n_kt - 1) >> 1) & 1, p.err);
+    // (the PV warp's last commit covers every earlier product too)
+    if (ok) ok = mbar_wait(&bar_ve[(n_kt - 1) % NSB], ((n_kt - 1) / NSB) & 1, p.err);
     if (ok) {
       red_l[ch][r] = l;
       __syncwarp();

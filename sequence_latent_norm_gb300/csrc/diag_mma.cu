@@ -33,23 +33,24 @@ constexpr int UNR = 48;
 
 // FORM 0: A and B in shared memory; 1: A in TMEM; 2: alternating 0 and 1.
 // BMN: B is MN-major (N in 64-wide boxes 16 KB apart) instead of K-major.
-// BG: while the MMAs run, warps 1-3 0: idle; 1: stream tcgen05.ld from
+// BG: while the MMAs run, warps 1-7 (warp 4 shares the issuing warp's
+// scheduler) 0: idle; 1: stream tcgen05.ld from
 // other TMEM columns; 2: stream 16-byte shared-memory stores; 3: warp 1
 // streams 16 KB bulk copies (the TMA engine) from global into shared
 // memory, two in flight; 4: stream TMEM stores; 5: exponentials and FMAs
 // in registers.
 // Instruction k goes to accumulator (k / run) % n_acc at column acc * n.
 template <int FORM, int BMN, int BG>
-__global__ void __launch_bounds__(128, 1)
-    diag_mma_kernel(int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk,
+__global__ void __launch_bounds__(256, 1)
+    diag_mma_kernel(int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk, int two,
                     unsigned long long* cycles, int* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  __shared__ uint64_t bar, bg_bar[2];
+  __shared__ uint64_t bar, bar2, bg_bar[2];
   __shared__ uint32_t tmem_sh;
   __shared__ volatile int stop;
-  __shared__ float sink[4];
+  __shared__ float sink[8];
   __shared__ unsigned long long bg_cycles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // operands: small repeating values, or (rnd) values spread like N(0,1)
@@ -71,6 +72,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
+    mbar_init(&bar2, 1);
     mbar_init(&bg_bar[0], 1);
     mbar_init(&bg_bar[1], 1);
     fence_barrier_init();
@@ -90,13 +92,16 @@ __global__ void __launch_bounds__(128, 1)
     uint32_t z[16];
 #pragma unroll
     for (int k = 0; k < 16; ++k) z[k] = rnd ? 0xbf803f80u ^ (uint32_t)(k * 0x00110011u) : 0x3c003c00u;
-    tmem_st16(tmem_addr(tmem, warp, A_TMEM_COL), z);
-    tmem_wait_st();
+    if (warp < 4) {
+      tmem_st16(tmem_addr(tmem, warp, A_TMEM_COL), z);
+      tmem_wait_st();
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (threadIdx.x == 0) {
+  const int issuer = threadIdx.x >> 5;   // with `two`, lane 0 of warps 0 and 1 both issue
+  if (threadIdx.x == 0 || (two && threadIdx.x == 32)) {
     const uint32_t id = idesc_bf16(128, n, 0, BMN);
     const uint32_t ab = smem_u32(sm), bb = smem_u32(sm + A_BYTES);
     uint64_t ad[4], bd[4];
@@ -107,10 +112,12 @@ __global__ void __launch_bounds__(128, 1)
     }
     uint32_t d[UNR];
 #pragma unroll
-    for (int k = 0; k < UNR; ++k) d[k] = tmem + (uint32_t)(((k / run) % n_acc) * n);
+    for (int k = 0; k < UNR; ++k)
+      d[k] = tmem + (uint32_t)(((k / run) % n_acc) * n + issuer * n_acc * n);
     const uint32_t at0 = tmem + A_TMEM_COL, at1 = at0 + 8;
     const unsigned long long t0 = clock64();
-    for (int blk = 0; blk < n_blocks; ++blk) {
+    const int my_blocks = two ? n_blocks / 2 : n_blocks;
+    for (int blk = 0; blk < my_blocks; ++blk) {
 #pragma unroll
       for (int k = 0; k < UNR; ++k) {
         const bool ts = FORM == 1 || (FORM == 2 && (k & 1));
@@ -120,11 +127,14 @@ __global__ void __launch_bounds__(128, 1)
           mma_ss(d[k], ad[k & 3], bd[k & 3], id, 1u);
       }
     }
-    mma_commit(&bar);
-    const bool ok = mbar_wait(&bar, 0, err);
+    mma_commit(issuer == 0 ? &bar : &bar2);
+    bool ok = mbar_wait(issuer == 0 ? &bar : &bar2, 0, err);
+    if (two && issuer == 0) ok = mbar_wait(&bar2, 0, err) && ok;
     const unsigned long long t1 = clock64();
-    if (!bg_clk) cycles[blockIdx.x] = ok ? t1 - t0 : 0ull;
-    stop = 1;
+    if (issuer == 0) {
+      if (!bg_clk) cycles[blockIdx.x] = ok ? t1 - t0 : 0ull;
+      stop = 1;
+    }
   } else if (BG == 3 && warp == 1) {
     // background bulk copies until the MMAs are done (bounded)
     if (lane == 0) {
@@ -146,7 +156,7 @@ __global__ void __launch_bounds__(128, 1)
   } else if (BG == 6 && warp > 0) {
     // background broadcast shared-memory loads (every lane reads the same
     // 16 bytes), the pattern of per-column softmax statistics
-    const float4* src = reinterpret_cast<const float4*>(sm + BG_OFF + (warp - 1) * 8192);
+    const float4* src = reinterpret_cast<const float4*>(sm + BG_OFF + ((warp - 1) & 3) * 8192);
     float acc = 0.f;
     const unsigned long long b0 = clock64();
     uint32_t nops = 0;
@@ -177,7 +187,7 @@ __global__ void __launch_bounds__(128, 1)
     for (int k = 0; k < 16; ++k) v[k] = 0x3f803f80u + (uint32_t)k;
     for (uint32_t it = 0; it < (1u << 22) && !stop; ++it) {
       v[it & 15] += 1u;
-      tmem_st16(tmem_addr(tmem, warp, BG_TMEM_COL + (int)(it & 1) * 16), v);
+      tmem_st16(tmem_addr(tmem, warp & 3, BG_TMEM_COL + (int)(it & 1) * 16), v);
       tmem_wait_st();
     }
   } else if ((BG == 1 || BG == 2) && warp > 0) {
@@ -188,10 +198,10 @@ __global__ void __launch_bounds__(128, 1)
     for (uint32_t it = 0; it < (1u << 22) && !stop; ++it, ++nops) {
       if (BG == 1) {
         uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, warp, BG_TMEM_COL), u);
+        tmem_ld32(tmem_addr(tmem, warp & 3, BG_TMEM_COL), u);
         acc += __uint_as_float(u[it & 31]);
       } else {
-        uint4* dst = reinterpret_cast<uint4*>(sm + BG_OFF + (warp - 1) * 8192);
+        uint4* dst = reinterpret_cast<uint4*>(sm + BG_OFF + ((warp - 1) & 3) * 8192);
 #pragma unroll
         for (int k = 0; k < 4; ++k)
           dst[(k * 32 + lane + (int)(it & 3) * 128) & 511] = make_uint4(it, k, lane, warp);
@@ -211,42 +221,43 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 template <int FORM, int BMN, int BG>
-cudaError_t launch_diag(int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk, int n_cta,
+cudaError_t launch_diag(int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk, int two,
+                        int n_cta,
                         unsigned long long* cycles, int* err, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(diag_mma_kernel<FORM, BMN, BG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   if (e != cudaSuccess) return e;
-  diag_mma_kernel<FORM, BMN, BG><<<n_cta, 128, SMEM, st>>>(n, n_acc, run, n_blocks, rnd, bg_clk,
-                                                           cycles, err);
+  diag_mma_kernel<FORM, BMN, BG><<<n_cta, 256, SMEM, st>>>(n, n_acc, run, n_blocks, rnd, bg_clk,
+                                                           two, cycles, err);
   return cudaGetLastError();
 }
 
 template <int FORM, int BMN>
 cudaError_t launch_diag_bg(int bg, int n, int n_acc, int run, int n_blocks, int rnd, int bg_clk,
-                           int n_cta,
+                           int two, int n_cta,
                            unsigned long long* cycles, int* err, cudaStream_t st) {
   if (bg == 1)
-    return launch_diag<FORM, BMN, 1>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 1>(n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err, st);
   if (bg == 2)
-    return launch_diag<FORM, BMN, 2>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 2>(n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err, st);
   if (bg == 3)
-    return launch_diag<FORM, BMN, 3>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 3>(n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err, st);
   if (bg == 4)
-    return launch_diag<FORM, BMN, 4>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 4>(n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err, st);
   if (bg == 5)
-    return launch_diag<FORM, BMN, 5>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 5>(n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err, st);
   if (bg == 6)
-    return launch_diag<FORM, BMN, 6>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
-  return launch_diag<FORM, BMN, 0>(n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err, st);
+    return launch_diag<FORM, BMN, 6>(n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err, st);
+  return launch_diag<FORM, BMN, 0>(n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err, st);
 }
 
 template <int FORM>
 cudaError_t launch_diag_form(int bmn, int bg, int n, int n_acc, int run, int n_blocks, int rnd,
-                             int bg_clk, int n_cta, unsigned long long* cycles, int* err,
-                             cudaStream_t st) {
-  return bmn ? launch_diag_bg<FORM, 1>(bg, n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err,
+                             int bg_clk, int two, int n_cta, unsigned long long* cycles,
+                             int* err, cudaStream_t st) {
+  return bmn ? launch_diag_bg<FORM, 1>(bg, n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err,
                                        st)
-             : launch_diag_bg<FORM, 0>(bg, n, n_acc, run, n_blocks, rnd, bg_clk, n_cta, cycles, err,
+             : launch_diag_bg<FORM, 0>(bg, n, n_acc, run, n_blocks, rnd, bg_clk, two, n_cta, cycles, err,
                                        st);
 }
 
@@ -257,14 +268,16 @@ extern "C" laga_status laga_diag_mma_rate(int form, int n, int n_acc, int run, i
                                           int n_cta, unsigned long long* cycles, void* stream) {
   using namespace laga;
   const int op = form & 3, bmn = (form >> 2) & 1, bg = (form >> 3) & 7, rnd = (form >> 6) & 1;
-  const int bg_clk = (form >> 7) & 1;
-  if (form < 0 || form >= 256 || bg > 6 || (bg_clk && bg != 1 && bg != 2 && bg != 6) || op > 2 || n < 16 || n > 256 || n % 16 != 0 ||
+  const int bg_clk = (form >> 7) & 1, two = (form >> 8) & 1;
+  if (form < 0 || form >= 512 || (two && bg != 0) || bg > 6 || (bg_clk && bg != 1 && bg != 2 && bg != 6) || op > 2 || n < 16 || n > 256 || n % 16 != 0 ||
       n_acc < 1 || run < 1 || n_instr < 1 || n_instr > (1 << 20) || n_cta < 1 || n_cta > 4096 ||
       !cycles)
     return LAGA_ERR_ARG;
   if (bmn && n % 64 != 0) return LAGA_ERR_ARG;
   const int cols = (bg == 1 || bg == 4) ? BG_TMEM_COL : (op == 0 ? 512 : A_TMEM_COL);
-  if (n_acc * n > cols || n_instr % UNR != 0 || UNR % (n_acc * run) != 0) return LAGA_ERR_ARG;
+  if ((two + 1) * n_acc * n > cols || n_instr % ((two + 1) * UNR) != 0 ||
+      UNR % (n_acc * run) != 0)
+    return LAGA_ERR_ARG;
   if ((reinterpret_cast<uintptr_t>(cycles) & 7u) != 0) return LAGA_ERR_ALIGN;
   void* err = nullptr;
   if (cudaGetSymbolAddress(&err, g_diag_err) != cudaSuccess) return LAGA_ERR_CUDA;
@@ -272,8 +285,8 @@ extern "C" laga_status laga_diag_mma_rate(int form, int n, int n_acc, int run, i
   const int nb = n_instr / UNR;
   int* ew = static_cast<int*>(err);
   cudaError_t e =
-      op == 0   ? launch_diag_form<0>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, n_cta, cycles, ew, st)
-      : op == 1 ? launch_diag_form<1>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, n_cta, cycles, ew, st)
-                : launch_diag_form<2>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, n_cta, cycles, ew, st);
+      op == 0   ? launch_diag_form<0>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, two, n_cta, cycles, ew, st)
+      : op == 1 ? launch_diag_form<1>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, two, n_cta, cycles, ew, st)
+                : launch_diag_form<2>(bmn, bg, n, n_acc, run, nb, rnd, bg_clk, two, n_cta, cycles, ew, st);
   return e == cudaSuccess ? LAGA_OK : LAGA_ERR_CUDA;
 }
