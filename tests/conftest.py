@@ -45,6 +45,10 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
         tr.write_line(f"{w}: O max-abs {r['o_max_abs']:.2e} (over 1e-2: {r['o_flat_over']}/"
                       f"{r['o_n']}, storage-bound use {r['o_bound_use']:.2f}) rel-fro "
                       f"{r['o_rel_fro']:.2e}, LSE {r['lse_max_abs']:.1e}")
+    for w, r in RECORDS:
+        g = {k: v for k, v in r.items() if k in ("dq", "dc", "dw", "dgamma")}
+        if g:
+            tr.write_line(f"{w}: gradients rel-fro " + ", ".join(f"{k} {v:.2e}" for k, v in g.items()))
     grads = {}
     for w, r in RECORDS:
         for k, v in r.items():
