@@ -46,7 +46,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, help="workload configuration (default 2)")
-    ap.add_argument("--form", default="laga", choices=["laga", "explicit"])
+    ap.add_argument("--form", default="laga", choices=["laga", "explicit", "laga_fused"])
+    ap.add_argument("--no-fused-variant", action="store_true",
+                    help="skip the timing of the fused up-projection form beside the main line")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--seq", type=int, default=0,
@@ -166,6 +168,9 @@ def kernel_work(name: str, S: int, H: int, B: int = 1):
         # (whose recomputed S and dP are not counted)
         "attn_bwd_dkdv": ("tensor", pairs * (2 * 192 + 2 * 128 + 2 * 128 + 2 * 192)),
         "attn_bwd_dq": ("tensor", pairs * 2 * 192),
+        # the fused form's dK/dV kernel also rebuilds K/V = L W (1x the up-projection)
+        "attn_bwd_dkdv_fused": ("tensor", pairs * (2 * 192 + 2 * 128 + 2 * 128 + 2 * 192)
+                                + 2.0 * T * 512 * H * 256),
         "upproj": ("tensor", 2.0 * T * 512 * H * 256),
         "upproj_dw": ("tensor", 2.0 * T * 512 * H * 256),
         "upproj_dl": ("tensor", 2.0 * T * 512 * H * 256),
@@ -442,6 +447,9 @@ def run_ours(args, rank, world, local_rank):
                 "unit": "GB/s", "frac": round(ach / peak_gbs, 4),
                 "peak_source": f"{peak_src} HBM copy"}
     roof["traffic"] = ncu_traffic(top, base.name)
+    fused = None
+    if args.form == "laga" and not args.no_fused_variant:
+        fused = fused_variant(args, wl, t, dev, stream, flush, peak_tf)
     attn_ms = sum(prof[k][0] for k in prof if k.startswith("attn")) / args.steps
     up_f = 3 * 2.0 * B * S * 512 * H * 256
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -465,9 +473,62 @@ def run_ours(args, rank, world, local_rank):
             "clocks": clk,
             "e2e": e2e,
             "gpu_launches": launches[0] * args.steps,
-            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu_baseline}
+            "roofline": roof, "kernels": kernels, "cpu_baseline": cpu_baseline,
+            "fused_upproj_variant": fused}
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def fused_variant(args, wl, t, dev, stream, flush, peak_tf):
+    """The fused up-projection form on the same inputs: step time (fwd +
+    bwd, one stream), its dK/dV kernel's rate and the saved-activation
+    bytes of both forms."""
+    import torch
+    import sequence_latent_norm_gb300 as pkg
+    S, H, B = wl.S, wl.H, wl.B
+    shard = pkg.Shard(S=S, H=H, n_h_total=wl.n_h_total, head_offset=wl.head_offset, B=B,
+                      io_dtype=wl.dtype, form="laga_fused")
+    run = pkg.Laga(shard, device=dev)
+    base_dims = pkg.Shard(S=S, H=H, n_h_total=wl.n_h_total, head_offset=wl.head_offset, B=B,
+                          io_dtype=wl.dtype, form="laga").dims()
+
+    def step():
+        o, lse = run.forward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"])
+        run.backward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"], o, lse, t["dO"])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    pkg._lib.sync_check()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    pkg._lib.profile_reset()
+    pkg._lib.profile_enable(True)
+    for _ in range(args.steps):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(dev)
+    pkg._lib.profile_enable(False)
+    prof = pkg._lib.profile_read()
+    pkg._lib.sync_check()
+    k = "attn_bwd_dkdv_fused"
+    per = prof[k][0] / prof[k][1]
+    _, units = kernel_work(k, S, H, B)
+    fwd_f, bwd_f = attention_flops(S, H, B)
+    return {"form": "laga_fused", "ms_per_step": round(ms, 4),
+            "value": round((fwd_f + bwd_f) / (ms * 1e-3) / 1e12, 3), "unit": UNIT,
+            "dkdv_fused_ms_per_launch": round(per, 4),
+            "dkdv_fused_tflops": round(units / (per * 1e-3) / 1e12, 2),
+            "dkdv_fused_frac": round(units / (per * 1e-3) / 1e12 / peak_tf, 4),
+            "saved_bytes": run.saved_bytes, "saved_bytes_laga": pkg._lib.workspace_bytes(base_dims, pkg._lib.WS_SAVED),
+            "fwd_scratch_bytes": run.fwd_bytes}
 
 
 # ----------------------------------------------------------------- sweep

@@ -66,7 +66,7 @@ typedef enum {
   LAGA_ERR_TIMEOUT = 6       /* a bounded device wait gave up                */
 } laga_status;
 
-/* Which of the three forms of Section 3 to run on one rank.
+/* Which form of Section 3 to run on one rank.
  *  LAGA      latent gathered, K/V rebuilt per head shard, K/V layout
  *            [B, S, H, d_nope + d_v] (token-major).
  *  EXPLICIT  same arithmetic, K/V in the head-major layout [B, H, S, ...]
@@ -74,8 +74,22 @@ typedef enum {
  *            at SP = 1 results are bit-identical to LAGA (Proposition 1).
  *  ABSORBED  q_absorbed = W^k^T q_nope, attention over the latent, latent
  *            accumulator, V up-projection afterwards (Section 3.2, B2); the
- *            memory-trap contrast path, not a performance path. */
-typedef enum { LAGA_FORM_LAGA = 0, LAGA_FORM_EXPLICIT = 1, LAGA_FORM_ABSORBED = 2 } laga_form;
+ *            memory-trap contrast path, not a performance path.
+ *  LAGA_FUSED  the LAGA form with the up-projection fused into the
+ *            key-stationary backward (the fused up-projection kernel the
+ *            paper leaves to future work, Section 4.7 and Section 8): the
+ *            dK/dV kernel rebuilds each key tile's k_nope and v from L and
+ *            W_kv_b on the tensor cores, so the forward's K/V is scratch
+ *            (LAGA_WS_FWD) instead of a saved activation, and LAGA_WS_SAVED
+ *            shrinks by B * S * n_h_shard * (d_nope + d_v) * 2 bytes (with
+ *            d_nope + d_v padded to 256).  Same arithmetic as LAGA: results
+ *            are identical to it. */
+typedef enum {
+  LAGA_FORM_LAGA = 0,
+  LAGA_FORM_EXPLICIT = 1,
+  LAGA_FORM_ABSORBED = 2,
+  LAGA_FORM_LAGA_FUSED = 3
+} laga_form;
 
 /* Normalisation of the latent (step a1).  The paper's "LN" is LayerNorm:
  * mean-subtracted, biased variance, gain gamma, no bias.  LAGA_NORM_RMS is
@@ -108,6 +122,9 @@ typedef struct {
 /* Workspace passes. */
 #define LAGA_WS_SAVED 0   /* written by laga_fwd, read by laga_bwd: keep it    */
 #define LAGA_WS_BWD 1     /* transient scratch of laga_bwd                     */
+#define LAGA_WS_FWD 2     /* transient scratch of laga_fwd_scratch: read and   */
+                          /* written only by that call's kernels (0 bytes     */
+                          /* except for LAGA_FORM_LAGA_FUSED)                 */
 
 /* Bytes of workspace `pass` needs for these dims (0 if the dims are
  * invalid).  Host-only, no CUDA call. */
@@ -132,6 +149,16 @@ laga_status laga_workspace_tensor(const laga_dims* dims, int pass, int index,
 laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
                      const float* gamma, const float* cos, const float* sin,
                      void* o, float* lse, void* ws_saved, size_t saved_bytes, void* stream);
+
+/* laga_fwd with a forward scratch: ws_fwd / fwd_bytes is a LAGA_WS_FWD
+ * workspace, free for other use once the call's kernels on `stream` are
+ * done.  ws_fwd may be NULL when laga_workspace_bytes(dims, LAGA_WS_FWD) is
+ * 0; LAGA_FORM_LAGA_FUSED needs it (laga_fwd returns LAGA_ERR_WORKSPACE for
+ * that form).  Otherwise as laga_fwd. */
+laga_status laga_fwd_scratch(const laga_dims* dims, const void* q, const void* c,
+                             const void* w_kvb, const float* gamma, const float* cos,
+                             const float* sin, void* o, float* lse, void* ws_saved,
+                             size_t saved_bytes, void* ws_fwd, size_t fwd_bytes, void* stream);
 
 /* Backward, steps a5-a7, for the loss sum(O * dO).
  *   q, c, w_kvb, gamma, cos, sin, o, lse: exactly as given to / returned by
@@ -166,8 +193,10 @@ laga_status laga_bwd(const laga_dims* dims, const void* q, const void* c, const 
  * caller enqueues on aux_stream afterwards follows the dQ kernel.  The
  * events and aux_stream must not be used by another call until this one's
  * work is enqueued (the library keeps no lock).  While per-kernel profiling
- * is on, every kernel runs on `stream`.  For the absorbed form this is
- * laga_bwd.  LAGA_ERR_ARG if an event is NULL or aux_stream == stream. */
+ * is on, every kernel runs on `stream`.  For the absorbed and fused forms
+ * this is laga_bwd (the fused form's dQ kernel reads the K/V that its dK/dV
+ * kernel rebuilds).  LAGA_ERR_ARG if an event is NULL or
+ * aux_stream == stream. */
 laga_status laga_bwd_overlap(const laga_dims* dims, const void* q, const void* c,
                              const void* w_kvb, const float* gamma, const float* cos,
                              const float* sin, const void* o, const float* lse, const void* d_o,

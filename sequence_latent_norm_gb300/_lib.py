@@ -16,12 +16,13 @@ LIB_PATH = os.path.join(PKG, "liblaga.so")
 
 LAGA_OK, LAGA_ERR_ARG, LAGA_ERR_ALIGN, LAGA_ERR_WORKSPACE = 0, 1, 2, 3
 LAGA_ERR_UNSUPPORTED, LAGA_ERR_CUDA, LAGA_ERR_TIMEOUT = 4, 5, 6
-FORMS = {"laga": 0, "explicit": 1, "absorbed": 2}
+FORMS = {"laga": 0, "explicit": 1, "absorbed": 2, "laga_fused": 3}
 DTYPES = {"bf16": 0, "fp32": 1}
 NORMS = {"layer": 0, "rms": 1}
-WS_SAVED, WS_BWD = 0, 1
+WS_SAVED, WS_BWD, WS_FWD = 0, 1, 2
 
-EXPORTED = ("laga_workspace_bytes", "laga_workspace_tensor", "laga_fwd", "laga_bwd",
+EXPORTED = ("laga_workspace_bytes", "laga_workspace_tensor", "laga_fwd", "laga_fwd_scratch",
+            "laga_bwd",
             "laga_bwd_overlap", "laga_sync_check", "laga_status_string", "laga_last_launch_count",
             "laga_profile_enable", "laga_profile_reset", "laga_profile_read",
             "laga_norm_rope_bwd_noalloc", "laga_selftest_wait_timeout", "laga_diag_mma_rate")
@@ -63,6 +64,8 @@ def load(path: str = LIB_PATH):
     lib.laga_workspace_tensor.restype = I
     lib.laga_fwd.argtypes = [D, P, P, P, P, P, P, P, P, P, S, P]
     lib.laga_fwd.restype = I
+    lib.laga_fwd_scratch.argtypes = [D, P, P, P, P, P, P, P, P, P, S, P, S, P]
+    lib.laga_fwd_scratch.restype = I
     lib.laga_bwd.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P, S, P]
     lib.laga_bwd.restype = I
     lib.laga_bwd_overlap.argtypes = [D, P, P, P, P, P, P, P, P, P, P, P, P, P, P, S, P, S, P,
@@ -128,6 +131,13 @@ def fwd(dims: LagaDims, q, c, w, gamma, cos, sin, o, lse, ws_saved, saved_bytes,
     """laga_fwd with raw device addresses (ints)."""
     _check(load().laga_fwd(ctypes.byref(dims), q, c, w, gamma, cos, sin, o, lse, ws_saved,
                            saved_bytes, stream), "laga_fwd")
+
+
+def fwd_scratch(dims: LagaDims, q, c, w, gamma, cos, sin, o, lse, ws_saved, saved_bytes, ws_fwd,
+                fwd_bytes, stream=0):
+    """laga_fwd_scratch with raw device addresses (ints)."""
+    _check(load().laga_fwd_scratch(ctypes.byref(dims), q, c, w, gamma, cos, sin, o, lse, ws_saved,
+                                   saved_bytes, ws_fwd, fwd_bytes, stream), "laga_fwd_scratch")
 
 
 def bwd(dims: LagaDims, q, c, w, gamma, cos, sin, o, lse, d_o, dq, dc, dw, dgamma, ws_saved,

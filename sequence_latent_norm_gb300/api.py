@@ -32,7 +32,7 @@ class Shard:
     scale: float = 0.0
     ln_eps: float = 1e-5
     io_dtype: str = "bf16"
-    form: str = "laga"
+    form: str = "laga"       # "laga", "laga_fused", "explicit" or "absorbed"
     norm: str = "layer"      # latent norm: "layer" (LayerNorm) or "rms" (its RMS variant)
 
     def dims(self) -> _lib.LagaDims:
@@ -82,6 +82,7 @@ class Laga:
         self.c_dims = shard.dims()
         self.saved_bytes = _lib.workspace_bytes(self.c_dims, _lib.WS_SAVED)
         self.bwd_bytes = _lib.workspace_bytes(self.c_dims, _lib.WS_BWD)
+        self.fwd_bytes = _lib.workspace_bytes(self.c_dims, _lib.WS_FWD)
         if self.saved_bytes == 0:
             raise ValueError(f"invalid shard dims {shard}")
         self.ws_saved = torch.empty(self.saved_bytes, dtype=torch.uint8, device=self.device)
@@ -119,8 +120,16 @@ class Laga:
         if lse is None:
             lse = torch.empty(shp["lse"], dtype=torch.float32, device=self.device)
         p = self._ptrs(q=q, c=c, w=w, gamma=gamma, cos=cos, sin=sin, o=o, lse=lse)
-        _lib.fwd(self.c_dims, p["q"], p["c"], p["w"], p["gamma"], p["cos"], p["sin"], p["o"],
-                 p["lse"], self.ws_saved.data_ptr(), self.saved_bytes, _stream_handle(stream))
+        # the forward scratch (the fused form's K/V) is released on return:
+        # the caching allocator hands it out again only in stream order
+        scratch = (torch.empty(self.fwd_bytes, dtype=torch.uint8, device=self.device)
+                   if self.fwd_bytes else None)
+        if scratch is not None and stream is not None:
+            scratch.record_stream(stream)
+        _lib.fwd_scratch(self.c_dims, p["q"], p["c"], p["w"], p["gamma"], p["cos"], p["sin"],
+                         p["o"], p["lse"], self.ws_saved.data_ptr(), self.saved_bytes,
+                         scratch.data_ptr() if scratch is not None else 0, self.fwd_bytes,
+                         _stream_handle(stream))
         return o, lse
 
     def _overlap_events(self):

@@ -98,7 +98,10 @@ Views make_views(const Plan& p, const Ptrs& x) {
   v.qr = x.buf<__nv_bfloat16>(p, W_QR);
   v.L = x.buf<__nv_bfloat16>(p, W_L);
   v.kpe = x.buf<__nv_bfloat16>(p, W_KPE);
-  v.kv = x.buf<__nv_bfloat16>(p, W_KV);
+  // The fused form keeps no K/V between the passes: the forward's lives in
+  // its scratch, the backward's is rebuilt by the dK/dV kernel.
+  v.kv = !p.fused ? x.buf<__nv_bfloat16>(p, W_KV)
+                  : x.buf<__nv_bfloat16>(p, x.ws_bwd ? T_KV : F_KV);
   const long long S = p.S, H = p.H;
   if (p.d.form == LAGA_FORM_EXPLICIT) {  // head-major [B, H, S, 256]
     v.kv_sb = H * S * DH; v.kv_ss = DH; v.kv_sh = S * DH;
@@ -134,6 +137,7 @@ size_t laga_workspace_bytes(const laga_dims* dims, int pass) {
   if (make_plan(dims, &p) != LAGA_OK) return 0;
   if (pass == LAGA_WS_SAVED) return p.saved_bytes;
   if (pass == LAGA_WS_BWD) return p.bwd_bytes;
+  if (pass == LAGA_WS_FWD) return p.fwd_bytes;
   return 0;
 }
 
@@ -143,8 +147,10 @@ laga_status laga_workspace_tensor(const laga_dims* dims, int pass, int index, co
   laga_status s = make_plan(dims, &p);
   if (s != LAGA_OK) return s;
   if (!name || !offset || !bytes || index < 0) return LAGA_ERR_ARG;
-  const int lo = pass == LAGA_WS_SAVED ? 0 : (pass == LAGA_WS_BWD ? N_SAVED : -1);
-  const int hi = pass == LAGA_WS_SAVED ? N_SAVED : N_BUF;
+  const int lo = pass == LAGA_WS_SAVED ? 0
+                 : pass == LAGA_WS_BWD ? N_SAVED
+                 : pass == LAGA_WS_FWD ? N_BWD_END : -1;
+  const int hi = pass == LAGA_WS_SAVED ? N_SAVED : pass == LAGA_WS_BWD ? N_BWD_END : N_BUF;
   if (lo < 0) return LAGA_ERR_ARG;
   int k = -1;
   for (int i = lo; i < hi; ++i) {
@@ -159,9 +165,10 @@ laga_status laga_workspace_tensor(const laga_dims* dims, int pass, int index, co
   return LAGA_ERR_ARG;
 }
 
-laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
-                     const float* gamma, const float* cos, const float* sin, void* o, float* lse,
-                     void* ws_saved, size_t saved_bytes, void* stream) {
+laga_status laga_fwd_scratch(const laga_dims* dims, const void* q, const void* c,
+                             const void* w_kvb, const float* gamma, const float* cos,
+                             const float* sin, void* o, float* lse, void* ws_saved,
+                             size_t saved_bytes, void* ws_fwd, size_t fwd_bytes, void* stream) {
   t_launches = 0;
   Plan p;
   laga_status s = make_plan(dims, &p);
@@ -172,11 +179,14 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
     if (!ptr) return LAGA_ERR_ARG;
   for (const void* ptr : ptrs)
     if (!aligned16(ptr)) return LAGA_ERR_ALIGN;
+  if (ws_fwd && !aligned16(ws_fwd)) return LAGA_ERR_ALIGN;
   if (saved_bytes < p.saved_bytes) return LAGA_ERR_WORKSPACE;
+  if (p.fwd_bytes > 0 && (!ws_fwd || fwd_bytes < p.fwd_bytes)) return LAGA_ERR_WORKSPACE;
   Ptrs x;
   x.q = q; x.c = c; x.w = w_kvb; x.gamma = gamma; x.cos = cos; x.sin = sin;
   x.o = o; x.lse = lse;
   x.ws_saved = static_cast<unsigned char*>(ws_saved);
+  x.ws_fwd = static_cast<unsigned char*>(ws_fwd);
   if ((s = err_word(&x.err)) != LAGA_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
@@ -190,6 +200,13 @@ laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const 
   }
   if (e == cudaSuccess && !p.canonical) e = launch_unpad_o(p, x, st);
   return cuda_status(e);
+}
+
+laga_status laga_fwd(const laga_dims* dims, const void* q, const void* c, const void* w_kvb,
+                     const float* gamma, const float* cos, const float* sin, void* o, float* lse,
+                     void* ws_saved, size_t saved_bytes, void* stream) {
+  return laga_fwd_scratch(dims, q, c, w_kvb, gamma, cos, sin, o, lse, ws_saved, saved_bytes,
+                          nullptr, 0, stream);
 }
 
 // The backward of one shard.  `aux` is either `st` (everything in stream
@@ -225,7 +242,7 @@ static laga_status bwd_impl(const laga_dims* dims, const void* q, const void* c,
   if ((s = err_word(&x.err)) != LAGA_OK) return s;
   // With per-kernel profiling on, every kernel runs in turn on `st` so that
   // each kernel's events time it alone.
-  const bool fork = !absorbed && aux != st && !g_prof_on;
+  const bool fork = !absorbed && !p.fused && aux != st && !g_prof_on;
   cudaError_t e = launch_bwd_pre(p, x, st);
   if (absorbed) {
     if (e == cudaSuccess) e = launch_absorbed_bwd(p, x, st);

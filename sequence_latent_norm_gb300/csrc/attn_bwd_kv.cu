@@ -25,6 +25,18 @@
 // [480,512); the k_pe part of dK for tile i goes to [416,480), the dP^T
 // columns phase B has read and left free.  Every mbarrier is waited phase
 // by phase, so parity waits are exact.
+//
+// Fused form (the up-projection fused into the attention backward, the
+// LAGA page's Section 4.7 and Section 8 future work): instead of loading
+// k_nope_j and v_j, the CTA rebuilds them, [k_nope | v]_j = L_j W_h
+// (M 128 keys, N 256, K 512), before its walk.  The producer streams L_j and
+// W_h in eight 64-wide K chunks through the two Q buffers (idle until the
+// walk), the issuer accumulates into TMEM [256,512) (the S^T and dP^T
+// columns, unused until the walk), and the compute warps round the tile to
+// bf16 into the K_j / V_j boxes -- the rounding the up-projection GEMM
+// applies -- from which the producer also stores it to HBM for the dQ
+// kernel.  The walk is unchanged.  Per CTA that is 33.5 MFLOP and 384 KB of
+// L2 reads, once per key tile: 1x the up-projection in total.
 #include "common.cuh"
 #include "kernels.h"
 #include "sm100.cuh"
@@ -49,9 +61,12 @@ constexpr int C_DV = 0, C_DK = 128, C_S = 256, C_DP = 384, C_DKR = C_DP + 32;
 constexpr uint32_t KV_BYTES = 5 * BOX;
 constexpr uint32_t Q_BYTES = 3 * BOX + 1024;    // Q_i + LSE_i + delta_i
 constexpr uint32_t DO_BYTES = 2 * BOX;
+constexpr int NCH = 512 / 64;            // fused form: K chunks of the rebuild
+constexpr int WBOX = 64 * 64 * 2;        // one 64 x 64 box of W_h (MN-major)
 
 struct KvMaps {
-  CUtensorMap qn, qr, kv, kpe, dO, lse, dlt;
+  CUtensorMap qn, qr, kv, kpe, dO, lse, dlt;   // fused form: kv is the store map of the rebuilt K/V
+  CUtensorMap lat, w;        // fused form: L rows (64 x 128 boxes), W_h (64 x 64 boxes)
   CUtensorMap dkv;           // dK_nope | dV rows, 64 x 128 bf16 boxes
   CUtensorMap dkpe;          // per-head k_pe part of dK, 32 x 128 fp32 boxes
 };
@@ -75,6 +90,7 @@ LAGA_DEVINL uint32_t packed_col(int base, int s) {
   return s < 4 ? base + 8 * s : base + 96 + 8 * (s - 4);
 }
 
+template <bool FUSED>
 __global__ void __launch_bounds__(THREADS, 1)
     attn_bwd_kv_kernel(const __grid_constant__ KvMaps tm, const KvParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -82,6 +98,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                            ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_kv, bar_q_full[2], bar_q_free[2], bar_do_full, bar_do_free;
   __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_dkr, bar_tfree, bar_fin;
+  __shared__ uint64_t bar_pfull[2], bar_pfree[2], bar_kvacc, bar_kvready;   // fused form
   __shared__ uint32_t tmem_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -100,6 +117,12 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_dkr, 1);
     mbar_init(&bar_tfree, N_COMPUTE);
     mbar_init(&bar_fin, 1);
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bar_pfull[k], 1);
+      mbar_init(&bar_pfree[k], 1);
+    }
+    mbar_init(&bar_kvacc, 1);
+    mbar_init(&bar_kvready, N_COMPUTE);
     fence_barrier_init();
   }
   if (warp == 9) {
@@ -128,13 +151,37 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (warp == 8) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
-      mbar_arrive_expect_tx(&bar_kv, KV_BYTES);
-      tma_load_4d(sm + K_OFF, &tm.kv, &bar_kv, 0, k0, h, b);
-      tma_load_4d(sm + K_OFF + BOX, &tm.kv, &bar_kv, 64, k0, h, b);
-      tma_load_3d(sm + K_OFF + 2 * BOX, &tm.kpe, &bar_kv, 0, k0, b);
-      tma_load_4d(sm + V_OFF, &tm.kv, &bar_kv, 128, k0, h, b);
-      tma_load_4d(sm + V_OFF + BOX, &tm.kv, &bar_kv, 192, k0, h, b);
-      for (int t = 0; t < n_i; ++t) {
+      bool ok = true;
+      if (FUSED) {
+        // the k_pe band of K_j; k_nope_j and v_j are rebuilt from L_j and
+        // W_h, streamed in K chunks through the two Q buffers
+        mbar_arrive_expect_tx(&bar_kv, BOX);
+        tma_load_3d(sm + K_OFF + 2 * BOX, &tm.kpe, &bar_kv, 0, k0, b);
+        for (int c = 0; c < NCH; ++c) {
+          const int st = c & 1;
+          if (c >= 2 && !mbar_wait(&bar_pfree[st], ((c >> 1) - 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* a = sm + Q_OFF + st * 3 * BOX;
+          mbar_arrive_expect_tx(&bar_pfull[st], 3 * BOX);
+          tma_load_3d(a, &tm.lat, &bar_pfull[st], c * 64, k0, b);
+#pragma unroll
+          for (int n = 0; n < 4; ++n)
+            tma_load_2d(a + BOX + n * WBOX, &tm.w, &bar_pfull[st], h * 256 + n * 64, c * 64);
+        }
+        // the rebuild's MMAs have read both buffers before Q_0 and Q_1 land
+        ok = ok && mbar_wait(&bar_pfree[0], ((NCH >> 1) - 1) & 1, p.err) &&
+             mbar_wait(&bar_pfree[1], ((NCH >> 1) - 1) & 1, p.err);
+      } else {
+        mbar_arrive_expect_tx(&bar_kv, KV_BYTES);
+        tma_load_4d(sm + K_OFF, &tm.kv, &bar_kv, 0, k0, h, b);
+        tma_load_4d(sm + K_OFF + BOX, &tm.kv, &bar_kv, 64, k0, h, b);
+        tma_load_3d(sm + K_OFF + 2 * BOX, &tm.kpe, &bar_kv, 0, k0, b);
+        tma_load_4d(sm + V_OFF, &tm.kv, &bar_kv, 128, k0, h, b);
+        tma_load_4d(sm + V_OFF + BOX, &tm.kv, &bar_kv, 192, k0, h, b);
+      }
+      for (int t = 0; ok && t < n_i; ++t) {
         const int q0 = (j + t) * BT;
         const int qb = t & 1;
         // Q_i, LSE_i, delta_i into buffer i%2 once the dK MMAs of tile i-2
@@ -153,7 +200,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_arrive_expect_tx(&bar_do_full, DO_BYTES);
         tma_load_4d(sm + DO_OFF, &tm.dO, &bar_do_full, 0, h, q0, b);
         tma_load_4d(sm + DO_OFF + BOX, &tm.dO, &bar_do_full, 64, h, q0, b);
+        if (FUSED && t == 0) {
+          // the rebuilt k_nope_j | v_j to HBM, where the dQ kernel reads it;
+          // the boxes stay unchanged for the rest of the CTA
+          if (!mbar_wait(&bar_kvready, 0, p.err)) break;
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx) {
+            tma_store_4d(&tm.kv, sm + K_OFF + bx * BOX, bx * 64, k0, h, b);
+            tma_store_4d(&tm.kv, sm + V_OFF + bx * BOX, 128 + bx * 64, k0, h, b);
+          }
+          bulk_commit();
+        }
       }
+      if (FUSED) bulk_wait0();
     }
   } else if (warp == 9) {
     // ------------------------------------------------------------- MMA issuer
@@ -187,7 +246,30 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         mma_commit(&bar_s);
       };
-      bool ok = mbar_wait(&bar_kv, 0, p.err) && issue_s_nope(0);
+      bool ok = true;
+      if (FUSED) {
+        // [k_nope | v]_j = L_j W_h into [256,512): 8 chunks x 4 K-steps
+        const uint32_t idUP = idesc_bf16(128, 256, 0, 1);
+        for (int c = 0; c < NCH; ++c) {
+          const int st = c & 1;
+          if (!mbar_wait(&bar_pfull[st], (c >> 1) & 1, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a = smem_u32(sm + Q_OFF + st * 3 * BOX);
+          const uint32_t alo = sdesc_lo(a, 16), blo = sdesc_lo(a + BOX, WBOX);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + C_S, sdesc_make(alo + kk * (32 >> 4)),
+                   sdesc_make(blo + kk * (2048 >> 4)), idUP, (c > 0 || kk > 0) ? 1u : 0u);
+          mma_commit(&bar_pfree[st]);
+        }
+        if (ok) mma_commit(&bar_kvacc);
+        // the compute warps have read the accumulator and written K_j, V_j
+        ok = ok && mbar_wait(&bar_kvready, 0, p.err);
+      }
+      ok = ok && mbar_wait(&bar_kv, 0, p.err) && issue_s_nope(0);
       if (ok) issue_s_rope(0);
       for (int t = 0; ok && t < n_i; ++t) {
         const uint32_t qlo_mn = sdesc_lo(smem_u32(sm + Q_OFF + (t & 1) * 3 * BOX), BOX);
@@ -246,7 +328,37 @@ __global__ void __launch_bounds__(THREADS, 1)
     float acc[32];                      // this thread's 32 columns of the k_pe part of dK
 #pragma unroll
     for (int k = 0; k < 32; ++k) acc[k] = 0.f;
-    for (int t = 0; t < n_i; ++t) {
+    bool live = true;
+    if (FUSED) {
+      // the rebuilt k_nope_j (half 0) or v_j (half 1) rows, rounded to
+      // bf16, into the 128-byte swizzled K_j / V_j boxes
+      live = mbar_wait(&bar_kvacc, 0, p.err);
+      if (live) {
+        tc_fence_after();
+        uint8_t* dst = sm + (ch == 0 ? K_OFF : V_OFF);
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t u[32];
+          tmem_ld32(tmem_addr(tmem, qd, C_S + ch * 128 + cc * 32), u);
+          uint8_t* row = dst + (cc >> 1) * BOX + r * 128;
+          const int g0 = (cc & 1) * 4;
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            uint4 w;
+            w.x = pack_bf16(__uint_as_float(u[8 * g]), __uint_as_float(u[8 * g + 1]));
+            w.y = pack_bf16(__uint_as_float(u[8 * g + 2]), __uint_as_float(u[8 * g + 3]));
+            w.z = pack_bf16(__uint_as_float(u[8 * g + 4]), __uint_as_float(u[8 * g + 5]));
+            w.w = pack_bf16(__uint_as_float(u[8 * g + 6]), __uint_as_float(u[8 * g + 7]));
+            *reinterpret_cast<uint4*>(row + (((g0 + g) ^ (r & 7)) << 4)) = w;
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_kvready);
+      }
+    }
+    for (int t = 0; live && t < n_i; ++t) {
       const int i = j + t, q0 = i * BT;
       const float* lse_s = reinterpret_cast<const float*>(sm + LD_OFF + (t & 1) * 1024);
       const float* dlt_s = lse_s + 128;
@@ -452,6 +564,21 @@ cudaError_t launch_attn_bwd_kv(const Plan& p, const Ptrs& x, cudaStream_t st) {
     if ((e = make_tmap_f32(&tm.dkpe, x.buf<float>(p, T_DKPE), 4, dims, str, box, true)) != cudaSuccess)
       return e;
   }
+  if (p.fused) {
+    {
+      uint64_t dims[3] = {512, S, B}, str[2] = {1024, S * 1024};
+      uint32_t box[3] = {64, 128, 1};
+      if ((e = make_tmap_bf16(&tm.lat, v.L, 3, dims, str, box)) != cudaSuccess) return e;
+    }
+    {
+      uint64_t dims[2] = {H * 256, 512}, str[1] = {(uint64_t)v.w_ld * 2};
+      uint32_t box[2] = {64, 64};
+      if ((e = make_tmap_bf16(&tm.w, v.W, 2, dims, str, box)) != cudaSuccess) return e;
+    }
+  } else {
+    tm.lat = tm.kv;   // unused
+    tm.w = tm.kv;
+  }
   KvParams prm;
   prm.S = p.S;
   prm.H = p.H;
@@ -465,12 +592,12 @@ cudaError_t launch_attn_bwd_kv(const Plan& p, const Ptrs& x, cudaStream_t st) {
   prm.kv_sh = v.kv_sh;
   prm.dkpe = x.buf<float>(p, T_DKPE);
   prm.err = x.err;
-  e = cudaFuncSetAttribute(attn_bwd_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           SMEM_BYTES);
+  auto* kernel = p.fused ? attn_bwd_kv_kernel<true> : attn_bwd_kv_kernel<false>;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)prm.n_t * p.H * p.B;
-  LaunchScope ls_("attn_bwd_dkdv", st);
-  attn_bwd_kv_kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(tm, prm);
+  LaunchScope ls_(p.fused ? "attn_bwd_dkdv_fused" : "attn_bwd_dkdv", st);
+  kernel<<<(unsigned)grid, THREADS, SMEM_BYTES, st>>>(tm, prm);
   return cudaGetLastError();
 }
 

@@ -25,11 +25,12 @@ struct Ptrs {
   float* dgamma = nullptr;
   unsigned char* ws_saved = nullptr;
   unsigned char* ws_bwd = nullptr;
+  unsigned char* ws_fwd = nullptr;   // forward scratch (fused form)
   int* err = nullptr;  // device error word
 
   template <typename T>
   T* buf(const Plan& p, int id) const {
-    unsigned char* base = id < N_SAVED ? ws_saved : ws_bwd;
+    unsigned char* base = id < N_SAVED ? ws_saved : (id < N_BWD_END ? ws_bwd : ws_fwd);
     return reinterpret_cast<T*>(base + p.off[id]);
   }
 };

@@ -18,7 +18,8 @@ enum BufId {
   W_RSTD,       // fp32 [B*S]           LayerNorm 1/sqrt(var + eps)
   W_KPE,        // bf16 [B*S, 64]       RoPE'd k_pe (shared by all heads)
   W_QR,         // bf16 [B*S*H, 64]     RoPE'd q_rope
-  W_KV,         // bf16 [B*S*H, 256]    k_nope | v per head (LAGA/explicit)
+  W_KV,         // bf16 [B*S*H, 256]    k_nope | v per head (LAGA/explicit; not
+                //                      kept by the fused form)
   W_QABS,       // bf16 [B*S*H, 512]    q_absorbed (absorbed form)
   W_OLAT,       // bf16 [B*S*H, 512]    latent accumulator (absorbed form)
   W_QN,         // bf16 [B*S*H, 128]    padded q_nope (non-canonical dims / fp32)
@@ -38,6 +39,10 @@ enum BufId {
   T_DOLAT,      // bf16 [B*S*H, 512]    dO up-projected to the latent (absorbed)
   T_DQABS,      // fp32 [B*S*H, 512]    gradient of q_absorbed (absorbed)
   T_DWP,        // fp32 [splits, 512, H*256] split-K partials of dW
+  T_KV,         // bf16 [B*S*H, 256]    fused form: K/V rebuilt by the dK/dV kernel
+  N_BWD_END,
+  // transient of the forward (LAGA_WS_FWD)
+  F_KV = N_BWD_END,  // bf16 [B*S*H, 256] fused form: the forward's K/V
   N_BUF
 };
 
@@ -50,10 +55,11 @@ struct Plan {
   bool canonical = false;   // dims are 128/64/128/512 and I/O is bf16
   bool fp32 = false;
   bool rms = false;         // RMS variant of the latent norm (no mean subtraction)
+  bool fused = false;       // LAGA_FORM_LAGA_FUSED: K/V rebuilt in the dK/dV kernel
   float scale = 0.f;
   size_t off[N_BUF] = {};
   size_t len[N_BUF] = {};
-  size_t saved_bytes = 0, bwd_bytes = 0;
+  size_t saved_bytes = 0, bwd_bytes = 0, fwd_bytes = 0;
 
   long long tokens() const { return (long long)B * S; }
   long long rows() const { return (long long)B * S * H; }  // (token, head) rows
@@ -64,7 +70,7 @@ static const char* const kBufName[N_BUF] = {
     "L", "ln_mean", "ln_rstd", "k_pe_rot", "q_rope_rot", "kv", "q_absorbed", "o_latent",
     "q_nope_padded", "w_kvb_padded", "o_padded",
     "delta", "lse_log2", "dO_padded", "dq_rot", "dkv", "dk_pe_heads", "dL", "dgamma_partials",
-    "dw_padded", "dO_latent", "dq_absorbed", "dw_split_partials"};
+    "dw_padded", "dO_latent", "dq_absorbed", "dw_split_partials", "kv_rebuilt", "kv"};
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -102,7 +108,8 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
     return LAGA_ERR_ARG;
   if (!(d.scale >= 0.f) || !(d.ln_eps > 0.f)) return LAGA_ERR_ARG;
   if (d.io_dtype != LAGA_BF16 && d.io_dtype != LAGA_FP32) return LAGA_ERR_ARG;
-  if (d.form != LAGA_FORM_LAGA && d.form != LAGA_FORM_EXPLICIT && d.form != LAGA_FORM_ABSORBED)
+  if (d.form != LAGA_FORM_LAGA && d.form != LAGA_FORM_EXPLICIT && d.form != LAGA_FORM_ABSORBED &&
+      d.form != LAGA_FORM_LAGA_FUSED)
     return LAGA_ERR_ARG;
   if (d.norm != LAGA_NORM_LAYER && d.norm != LAGA_NORM_RMS) return LAGA_ERR_ARG;
   if (d.causal != 1) return LAGA_ERR_UNSUPPORTED;
@@ -114,6 +121,7 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
   p->dn = d.d_nope; p->dr = d.d_rope; p->dv = d.d_v; p->dkv = d.d_kv;
   p->fp32 = d.io_dtype == LAGA_FP32;
   p->rms = d.norm == LAGA_NORM_RMS;
+  p->fused = d.form == LAGA_FORM_LAGA_FUSED;
   p->canonical = !p->fp32 && d.d_nope == 128 && d.d_rope == 64 && d.d_v == 128 && d.d_kv == 512;
   p->scale = d.scale > 0.f ? d.scale : 1.0f / sqrtf((float)(d.d_nope + d.d_rope));
 
@@ -125,7 +133,7 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
   p->len[W_RSTD] = T * 4;
   p->len[W_KPE] = T * 64 * 2;
   p->len[W_QR] = R * 64 * 2;
-  if (!absorbed) p->len[W_KV] = R * 256 * 2;
+  if (!absorbed && !p->fused) p->len[W_KV] = R * 256 * 2;
   if (absorbed) { p->len[W_QABS] = R * 512 * 2; p->len[W_OLAT] = R * 512 * 2; }
   if (!p->canonical) {
     p->len[W_QN] = R * 128 * 2;
@@ -147,12 +155,19 @@ inline laga_status make_plan(const laga_dims* dims, Plan* p) {
   }
   const int splits = dw_splits(p->H, p->B * ((p->S + 63) / 64));
   if (!absorbed && splits > 1) p->len[T_DWP] = (size_t)splits * 512 * H * 256 * 4;
+  if (p->fused) {
+    p->len[T_KV] = R * 256 * 2;
+    p->len[F_KV] = R * 256 * 2;
+  }
   size_t o = 0;
   for (int i = 0; i < N_SAVED; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }
   p->saved_bytes = o;
   o = 0;
-  for (int i = N_SAVED; i < N_BUF; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }
+  for (int i = N_SAVED; i < N_BWD_END; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }
   p->bwd_bytes = o;
+  o = 0;
+  for (int i = N_BWD_END; i < N_BUF; ++i) { p->off[i] = o; o = align_up(o + p->len[i], 1024); }
+  p->fwd_bytes = o;
   return LAGA_OK;
 }
 

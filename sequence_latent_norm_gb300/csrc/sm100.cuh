@@ -133,6 +133,8 @@ LAGA_DEVINL void tma_store_3d(const void* tmap, const void* src, int x, int y, i
 LAGA_DEVINL void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until the committed bulk groups have finished reading shared memory.
 LAGA_DEVINL void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until the committed bulk groups have completed (global writes done).
+LAGA_DEVINL void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 LAGA_DEVINL void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

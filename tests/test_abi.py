@@ -128,3 +128,43 @@ def test_latent_norm_field_is_validated(lib):
     d = lib.make_dims(256, 2)
     d.norm = 2
     assert lib.workspace_bytes(d, lib.WS_SAVED) == 0
+
+
+def test_fused_form_moves_kv_from_saved_to_scratch(lib):
+    """The fused form (up-projection rebuilt inside the key-stationary
+    backward) keeps no per-head K/V between the passes: the saved workspace
+    loses exactly the B*S*H*256 bf16 "kv" tensor, which becomes the forward's
+    scratch, and the backward scratch gains one of the same size for the
+    rebuilt tiles.  Every other tensor is unchanged."""
+    for S, H, B in [(16384, 16, 1), (129, 3, 2), (32768, 32, 1)]:
+        la = lib.make_dims(S, H, B=B)
+        fu = lib.make_dims(S, H, B=B, form="laga_fused")
+        sv_la = dict((n, b) for n, _, b in lib.workspace_tensors(la, lib.WS_SAVED))
+        sv_fu = dict((n, b) for n, _, b in lib.workspace_tensors(fu, lib.WS_SAVED))
+        kv = B * S * H * 256 * 2
+        assert sv_la["kv"] == kv and "kv" not in sv_fu
+        assert sv_fu == {n: b for n, b in sv_la.items() if n != "kv"}
+        assert lib.workspace_tensors(fu, lib.WS_FWD) == [("kv", 0, kv)]
+        assert lib.workspace_bytes(fu, lib.WS_FWD) == kv + (-kv) % 1024
+        assert lib.workspace_tensors(la, lib.WS_FWD) == [] and lib.workspace_bytes(la, lib.WS_FWD) == 0
+        bw_la = dict((n, b) for n, _, b in lib.workspace_tensors(la, lib.WS_BWD))
+        bw_fu = dict((n, b) for n, _, b in lib.workspace_tensors(fu, lib.WS_BWD))
+        assert bw_fu.pop("kv_rebuilt") == kv and bw_fu == bw_la
+        assert lib.workspace_bytes(la, lib.WS_SAVED) - lib.workspace_bytes(fu, lib.WS_SAVED) >= kv
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="fake pointers are only safe without a GPU")
+def test_fused_form_forward_needs_its_scratch(lib):
+    """laga_fwd (no scratch) refuses the fused form; laga_fwd_scratch checks
+    the scratch's size and alignment before any CUDA call."""
+    so = lib.load()
+    d = lib.make_dims(256, 2, form="laga_fused")
+    nb = lib.workspace_bytes(d, lib.WS_SAVED)
+    fb = lib.workspace_bytes(d, lib.WS_FWD)
+    p = [0x10000 * (i + 1) for i in range(10)]
+    assert so.laga_fwd(ctypes.byref(d), *p[:9], nb, None) == lib.LAGA_ERR_WORKSPACE
+    fs = so.laga_fwd_scratch
+    assert fs(ctypes.byref(d), *p[:9], nb, None, fb, None) == lib.LAGA_ERR_WORKSPACE
+    assert fs(ctypes.byref(d), *p[:9], nb, p[9], fb - 1, None) == lib.LAGA_ERR_WORKSPACE
+    assert fs(ctypes.byref(d), *p[:9], nb, p[9] + 8, fb, None) == lib.LAGA_ERR_ALIGN
+    assert fs(ctypes.byref(d), *p[:9], nb, p[9], fb, None) == lib.LAGA_ERR_CUDA

@@ -69,11 +69,15 @@ def run_guarded(wl, form):
     g = {k: Guarded(_nbytes(*v), dev) for k, v in shapes.items()}
     saved = lib.workspace_bytes(dims, lib.WS_SAVED)
     bwd = lib.workspace_bytes(dims, lib.WS_BWD)
+    fwd = lib.workspace_bytes(dims, lib.WS_FWD)
     g["ws_saved"], g["ws_bwd"] = Guarded(saved, dev), Guarded(bwd, dev)
+    if fwd:
+        g["ws_fwd"] = Guarded(fwd, dev)
     st = torch.cuda.current_stream().cuda_stream
     P = {k: v.data_ptr() for k, v in t.items()}
-    lib.fwd(dims, P["q"], P["c"], P["w"], P["gamma"], P["cos"], P["sin"], g["O"].ptr(),
-            g["LSE"].ptr(), g["ws_saved"].ptr(), saved, st)
+    lib.fwd_scratch(dims, P["q"], P["c"], P["w"], P["gamma"], P["cos"], P["sin"], g["O"].ptr(),
+                    g["LSE"].ptr(), g["ws_saved"].ptr(), saved,
+                    g["ws_fwd"].ptr() if fwd else 0, fwd, st)
     lib.bwd(dims, P["q"], P["c"], P["w"], P["gamma"], P["cos"], P["sin"], g["O"].ptr(),
             g["LSE"].ptr(), P["dO"], g["dq"].ptr(), g["dc"].ptr(), g["dw"].ptr(),
             g["dgamma"].ptr(), g["ws_saved"].ptr(), saved, g["ws_bwd"].ptr(), bwd, st)
@@ -95,7 +99,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("form", ["laga", "explicit", "absorbed"])
+@pytest.mark.parametrize("form", ["laga", "explicit", "absorbed", "laga_fused"])
 @pytest.mark.parametrize("case", CASES, ids=lambda c: f"S{c['S']}")
 def test_guard_bands_v3_dims(case, form):
     wl = config(1, **case)
@@ -105,7 +109,7 @@ def test_guard_bands_v3_dims(case, form):
     check_grads(got, ref, where=f"{form} {case}")
 
 
-@pytest.mark.parametrize("form", ["laga", "absorbed"])
+@pytest.mark.parametrize("form", ["laga", "absorbed", "laga_fused"])
 @pytest.mark.parametrize("wl", [config(0), config(1, S=129, H=2, B=2, d_nope=64, d_rope=32,
                                                    d_v=64, d_kv=256)],
                          ids=["fp32-config0", "bf16-small-dims"])

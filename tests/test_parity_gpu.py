@@ -193,3 +193,56 @@ def test_rms_latent_norm_variant_matches_oracle(wl, form):
     ref = oracle_run(wl, cpu)
     check_forward(got, ref, f"rms {wl.name} S={wl.S}", form=form)
     check_grads(got, ref, where=f"rms {wl.name} S={wl.S}")
+
+
+FUSED_CASES = [
+    dict(S=200, H=2),                                # ragged tail
+    dict(S=1, H=1),                                  # a single token
+    dict(S=129, H=3, B=2),                           # batch > 1, one past a tile edge
+    dict(S=384, H=2, n_h_total=5, head_offset=3),    # shard inside a wider W_kv_b
+    dict(S=150, H=3, d_kv=256),                      # narrower latent (padded W and L)
+    dict(S=333, H=2, norm="rms"),                    # RMS latent norm
+    dict(S=4096, H=16),                              # the 4096-token, 16-head shard
+]
+
+
+@pytest.mark.parametrize("case", FUSED_CASES, ids=lambda c: "-".join(f"{k}{v}" for k, v in c.items()))
+def test_fused_upprojection_form_matches_oracle_and_equals_laga(case):
+    """The fused form rebuilds each key tile's k_nope | v = L_j W_h inside
+    the key-stationary backward instead of reading the forward's K/V.  The
+    rebuild accumulates the same 32 K-steps in the same order as the
+    up-projection GEMM and rounds to bf16 the same way, so every output is
+    bit-identical to the LAGA form; both are checked against the oracle."""
+    wl = config(1, **case)
+    cpu = make_inputs(wl)
+    got = gpu_run(wl, cpu, form="laga_fused")
+    ref = oracle_run(wl, cpu)
+    check_forward(got, ref, f"fused {case}")
+    check_grads(got, ref, where=f"fused {case}")
+    base = gpu_run(wl, cpu, form="laga")
+    for k in got:
+        assert torch.equal(got[k], base[k]), f"fused form differs from LAGA in {k}"
+
+
+def test_fused_form_fp32_config_equals_laga():
+    wl = config(0)
+    cpu = make_inputs(wl)
+    got = gpu_run(wl, cpu, form="laga_fused")
+    check_forward(got, oracle_run(wl, cpu), "fused fp32-config0")
+    base = gpu_run(wl, cpu, form="laga")
+    for k in got:
+        assert torch.equal(got[k], base[k]), k
+
+
+@pytest.mark.parametrize("S,H", [(16384, 16), (32768, 32)])
+def test_fused_form_full_size_equals_laga(S, H):
+    """At the full shard (S=16384, 16 heads, the benchmarked launch) and at
+    the sweep's largest point (S=32768, 32 heads), where the LAGA form
+    itself is checked against the oracle: the fused form's outputs are
+    bit-identical to it."""
+    wl = config(2) if S == 16384 else config(4, S=S, H=H, n_h_total=H)
+    cpu = make_inputs(wl)
+    got = gpu_run(wl, cpu, form="laga_fused")
+    base = gpu_run(wl, cpu, form="laga")
+    for k in got:
+        assert torch.equal(got[k], base[k]), f"fused form differs from LAGA in {k} at S={S}"
