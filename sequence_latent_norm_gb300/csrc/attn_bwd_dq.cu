@@ -12,8 +12,9 @@
 //   warps 0-7  compute.  Warp w owns TMEM lane quadrant w%4 (query rows) and
 //              column half w/4 (key columns).  It reads S_ij into registers
 //              as P (freeing the S columns for S_i,j+1), then reads dP_ij and
-//              writes dS_ij as bf16 pairs packed into its own dP columns, the
-//              TMEM operand of the dQ MMA.
+//              writes dS_ij / scale as bf16 pairs packed into its own dP
+//              columns, the TMEM operand of the dQ MMA (dQ is scaled in the
+//              epilogue).
 //              First they place q_nope_i in TMEM as packed bf16 pairs, the
 //              TMEM A operand of the first 8 K-steps of S.
 //   warp 8     TMA producer: q_rope_i and dO_i once; K_j in a ring of three
@@ -265,8 +266,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_a);
-      // ---- dS_ij = P_ij (dP_ij - delta) * scale, packed into this warp's
-      //      own dP columns once it has read them
+      // ---- dS_ij / scale = P_ij (dP_ij - delta), packed into this warp's
+      //      own dP columns once it has read them (dQ is scaled once, in the
+      //      epilogue)
       if (!mbar_wait(&bar_dp, j & 1, p.err)) { ok = false; break; }
       tc_fence_after();
       // chunk c reads columns [32c, 32c+32) and writes [16c, 16c+16): the
@@ -277,9 +279,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(tmem_addr(tmem, qd, C_DP + ch * 64 + c * 32), ud);
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-          const float d0 = pv[c * 32 + 2 * k] * (__uint_as_float(ud[2 * k]) - dlt_r) * p.scale;
-          const float d1 =
-              pv[c * 32 + 2 * k + 1] * (__uint_as_float(ud[2 * k + 1]) - dlt_r) * p.scale;
+          const float d0 = pv[c * 32 + 2 * k] * (__uint_as_float(ud[2 * k]) - dlt_r);
+          const float d1 = pv[c * 32 + 2 * k + 1] * (__uint_as_float(ud[2 * k + 1]) - dlt_r);
           dk[k] = pack_bf16(d0, d1);
         }
         tmem_st16(tmem_addr(tmem, qd, C_DP + ch * 64 + c * 16), dk);
@@ -315,17 +316,24 @@ __global__ void __launch_bounds__(THREADS, 1)
             *reinterpret_cast<uint4*>(box + (((k0 + g) ^ (r & 7)) << 4)) = w;
           }
         };
+        const float sc = p.scale;
         {
           uint32_t u[32];
+          float v[32];
           tmem_ld32(tmem_addr(tmem, qd, C_DQ + ch * 96), u);
-          stage32(ch * 96, reinterpret_cast<const float*>(u));
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = sc * __uint_as_float(u[k]);
+          stage32(ch * 96, v);
         }
         if (ch == 0) {
 #pragma unroll 1
           for (int c = 1; c < 3; ++c) {
             uint32_t u[32];
+            float v[32];
             tmem_ld32(tmem_addr(tmem, qd, C_DQ + c * 32), u);
-            stage32(c * 32, reinterpret_cast<const float*>(u));
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = sc * __uint_as_float(u[k]);
+            stage32(c * 32, v);
           }
         } else {
           uint32_t ua[32], ub[32];
@@ -341,7 +349,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             const float cs[4] = {cv.x, cv.y, cv.z, cv.w}, sn[4] = {sv.x, sv.y, sv.z, sv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float av = __uint_as_float(ua[4 * k + e]), bv = __uint_as_float(ub[4 * k + e]);
+              const float av = sc * __uint_as_float(ua[4 * k + e]);
+              const float bv = sc * __uint_as_float(ub[4 * k + e]);
               ra[4 * k + e] = av * cs[e] + bv * sn[e];
               rb[4 * k + e] = bv * cs[e] - av * sn[e];
             }
@@ -361,8 +370,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              d4[k] = make_float4(__uint_as_float(u[4 * k]), __uint_as_float(u[4 * k + 1]),
-                                  __uint_as_float(u[4 * k + 2]), __uint_as_float(u[4 * k + 3]));
+              d4[k] = make_float4(p.scale * __uint_as_float(u[4 * k]),
+                                  p.scale * __uint_as_float(u[4 * k + 1]),
+                                  p.scale * __uint_as_float(u[4 * k + 2]),
+                                  p.scale * __uint_as_float(u[4 * k + 3]));
           }
         }
       }

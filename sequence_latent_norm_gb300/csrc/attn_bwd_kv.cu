@@ -11,8 +11,9 @@
 //   warps 0-7  compute.  Warp w owns TMEM lane quadrant w%4 (key rows) and
 //              column half w/4 (query columns).  Phase A: S^T -> P^T (bf16
 //              packed into its own S^T columns, the TMEM operand of dV).
-//              Phase B: dP^T -> dS^T * scale (bf16 packed into its own dP^T
-//              columns, the TMEM operand of dK).  Then it adds this tile's
+//              Phase B: dP^T -> dS^T / scale (bf16 packed into its own
+//              dP^T columns, the TMEM operand of dK; dK is scaled in the
+//              epilogue).  Then it adds this tile's
 //              k_pe part of dK from TMEM into registers.
 //   warp 8     TMA producer: K_j, V_j once; per i: Q_i with LSE_i and
 //              delta_i (double-buffered), dO_i.
@@ -30,9 +31,10 @@
 // LAGA page's Section 4.7 and Section 8 future work): instead of loading
 // k_nope_j and v_j, the CTA rebuilds them, [k_nope | v]_j = L_j W_h
 // (M 128 keys, N 256, K 512), before its walk.  The producer streams L_j and
-// W_h in eight 64-wide K chunks through the two Q buffers (idle until the
-// walk), the issuer accumulates into TMEM [256,512) (the S^T and dP^T
-// columns, unused until the walk), and the compute warps round the tile to
+// W_h in eight 64-wide K chunks through four buffers idle until the walk
+// (the Q, K_j, V_j and dO_i boxes), the issuer accumulates into TMEM
+// [256,512) (the S^T and dP^T columns, unused until the walk), and the
+// compute warps round the tile to
 // bf16 into the K_j / V_j boxes -- the rounding the up-projection GEMM
 // applies -- from which the producer also stores it to HBM for the dQ
 // kernel.  The walk is unchanged.  Per CTA that is 33.5 MFLOP and 384 KB of
@@ -62,7 +64,17 @@ constexpr uint32_t KV_BYTES = 5 * BOX;
 constexpr uint32_t Q_BYTES = 3 * BOX + 1024;    // Q_i + LSE_i + delta_i
 constexpr uint32_t DO_BYTES = 2 * BOX;
 constexpr int NCH = 512 / 64;            // fused form: K chunks of the rebuild
+constexpr int NST = 4;                   // fused form: chunk buffers
 constexpr int WBOX = 64 * 64 * 2;        // one 64 x 64 box of W_h (MN-major)
+// Buffers of the rebuild's chunks (an L box, and four W boxes of 8 KB in a
+// row), in regions idle until the walk: the two Q buffers, the K_j boxes
+// (the k_pe box is loaded after the rebuild) and the V_j / dO_i boxes.
+LAGA_DEVINL int chunk_a(int st) {
+  return st == 0 ? Q_OFF : st == 1 ? Q_OFF + 3 * BOX : st == 2 ? K_OFF + 2 * BOX : DO_OFF;
+}
+LAGA_DEVINL int chunk_b(int st) {
+  return st == 0 ? Q_OFF + BOX : st == 1 ? Q_OFF + 4 * BOX : st == 2 ? K_OFF : V_OFF;
+}
 
 struct KvMaps {
   CUtensorMap qn, qr, kv, kpe, dO, lse, dlt;   // fused form: kv is the store map of the rebuilt K/V
@@ -98,7 +110,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                            ~static_cast<uintptr_t>(1023));
   __shared__ uint64_t bar_kv, bar_q_full[2], bar_q_free[2], bar_do_full, bar_do_free;
   __shared__ uint64_t bar_s, bar_dp, bar_p, bar_ds, bar_dkr, bar_tfree, bar_fin;
-  __shared__ uint64_t bar_pfull[2], bar_pfree[2], bar_kvacc, bar_kvready;   // fused form
+  __shared__ uint64_t bar_pfull[NST], bar_pfree[NST], bar_kvacc, bar_kvready;   // fused form
   __shared__ uint32_t tmem_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -117,7 +129,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_dkr, 1);
     mbar_init(&bar_tfree, N_COMPUTE);
     mbar_init(&bar_fin, 1);
-    for (int k = 0; k < 2; ++k) {
+    for (int k = 0; k < NST; ++k) {
       mbar_init(&bar_pfull[k], 1);
       mbar_init(&bar_pfree[k], 1);
     }
@@ -153,26 +165,29 @@ __global__ void __launch_bounds__(THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       if (FUSED) {
-        // the k_pe band of K_j; k_nope_j and v_j are rebuilt from L_j and
-        // W_h, streamed in K chunks through the two Q buffers
-        mbar_arrive_expect_tx(&bar_kv, BOX);
-        tma_load_3d(sm + K_OFF + 2 * BOX, &tm.kpe, &bar_kv, 0, k0, b);
+        // k_nope_j and v_j are rebuilt from L_j and W_h, streamed in K
+        // chunks through four idle buffers
         for (int c = 0; c < NCH; ++c) {
-          const int st = c & 1;
-          if (c >= 2 && !mbar_wait(&bar_pfree[st], ((c >> 1) - 1) & 1, p.err)) {
+          const int st = c % NST;
+          if (c >= NST && !mbar_wait(&bar_pfree[st], ((c / NST) - 1) & 1, p.err)) {
             ok = false;
             break;
           }
-          uint8_t* a = sm + Q_OFF + st * 3 * BOX;
           mbar_arrive_expect_tx(&bar_pfull[st], 3 * BOX);
-          tma_load_3d(a, &tm.lat, &bar_pfull[st], c * 64, k0, b);
+          tma_load_3d(sm + chunk_a(st), &tm.lat, &bar_pfull[st], c * 64, k0, b);
 #pragma unroll
           for (int n = 0; n < 4; ++n)
-            tma_load_2d(a + BOX + n * WBOX, &tm.w, &bar_pfull[st], h * 256 + n * 64, c * 64);
+            tma_load_2d(sm + chunk_b(st) + n * WBOX, &tm.w, &bar_pfull[st], h * 256 + n * 64,
+                        c * 64);
         }
-        // the rebuild's MMAs have read both buffers before Q_0 and Q_1 land
-        ok = ok && mbar_wait(&bar_pfree[0], ((NCH >> 1) - 1) & 1, p.err) &&
-             mbar_wait(&bar_pfree[1], ((NCH >> 1) - 1) & 1, p.err);
+        // the rebuild's MMAs have read every buffer before the walk's
+        // operands and the k_pe band of K_j land there
+        for (int st = 0; ok && st < NST; ++st)
+          ok = mbar_wait(&bar_pfree[st], ((NCH / NST) - 1) & 1, p.err);
+        if (ok) {
+          mbar_arrive_expect_tx(&bar_kv, BOX);
+          tma_load_3d(sm + K_OFF + 2 * BOX, &tm.kpe, &bar_kv, 0, k0, b);
+        }
       } else {
         mbar_arrive_expect_tx(&bar_kv, KV_BYTES);
         tma_load_4d(sm + K_OFF, &tm.kv, &bar_kv, 0, k0, h, b);
@@ -251,14 +266,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         // [k_nope | v]_j = L_j W_h into [256,512): 8 chunks x 4 K-steps
         const uint32_t idUP = idesc_bf16(128, 256, 0, 1);
         for (int c = 0; c < NCH; ++c) {
-          const int st = c & 1;
-          if (!mbar_wait(&bar_pfull[st], (c >> 1) & 1, p.err)) {
+          const int st = c % NST;
+          if (!mbar_wait(&bar_pfull[st], (c / NST) & 1, p.err)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = smem_u32(sm + Q_OFF + st * 3 * BOX);
-          const uint32_t alo = sdesc_lo(a, 16), blo = sdesc_lo(a + BOX, WBOX);
+          const uint32_t alo = sdesc_lo(smem_u32(sm + chunk_a(st)), 16);
+          const uint32_t blo = sdesc_lo(smem_u32(sm + chunk_b(st)), WBOX);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
             mma_ss(tmem + C_S, sdesc_make(alo + kk * (32 >> 4)),
@@ -297,7 +312,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // S^T_{i+1} overwrites P^T_i only after the dV MMAs above read it.
         // Its k_nope steps keep the pipe busy until dS^T_i is ready; the
         // k_pe part of dK for tile i goes ahead of its k_pe steps, so the
-        // compute warps can read it out while the rest of the pipe runs.
+        // compute warps can read it out while the rest of the pipe runs
+        // (issuing all of S^T_{i+1} first was measured slower).
         if (next && !issue_s_nope(t + 1)) break;
         if (!mbar_wait(&bar_ds, t & 1, p.err)) break;
         tc_fence_after();
@@ -388,10 +404,12 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             const float4 l = lz[k];
-            pv[kk * 32 + 4 * k] = ex2(fmaf(__uint_as_float(us[4 * k]), p.sl2, -l.x));
-            pv[kk * 32 + 4 * k + 1] = ex2(fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -l.y));
-            pv[kk * 32 + 4 * k + 2] = ex2(fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -l.z));
-            pv[kk * 32 + 4 * k + 3] = ex2(fmaf(__uint_as_float(us[4 * k + 3]), p.sl2, -l.w));
+            float* o = pv + kk * 32 + 4 * k;
+            const float x0 = fmaf(__uint_as_float(us[4 * k]), p.sl2, -l.x);
+            const float x1 = fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -l.y);
+            const float x2 = fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -l.z);
+            const float x3 = fmaf(__uint_as_float(us[4 * k + 3]), p.sl2, -l.w);
+            o[0] = ex2(x0); o[1] = ex2(x1); o[2] = ex2(x2); o[3] = ex2(x3);
           }
         } else {
 #pragma unroll
@@ -412,8 +430,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p);
-      // ---- phase B: dS^T = P^T (dP^T - delta) * scale, packed like P^T
-      //      into the ends of the dP^T columns
+      // ---- phase B: dS^T / scale = P^T (dP^T - delta), packed like P^T
+      //      into the ends of the dP^T columns (dK is scaled once, in the
+      //      epilogue)
       if (!mbar_wait(&bar_dp, t & 1, p.err)) break;
       tc_fence_after();
 #pragma unroll
@@ -432,9 +451,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           const float4 dl = dz[k];
           const float* u = reinterpret_cast<const float*>(ud) + 4 * k;
           const float* pk = pv + kk * 32 + 4 * k;
-          dk[2 * k] = pack_bf16(pk[0] * (u[0] - dl.x) * p.scale, pk[1] * (u[1] - dl.y) * p.scale);
-          dk[2 * k + 1] =
-              pack_bf16(pk[2] * (u[2] - dl.z) * p.scale, pk[3] * (u[3] - dl.w) * p.scale);
+          dk[2 * k] = pack_bf16(pk[0] * (u[0] - dl.x), pk[1] * (u[1] - dl.y));
+          dk[2 * k + 1] = pack_bf16(pk[2] * (u[2] - dl.z), pk[3] * (u[3] - dl.w));
         }
         tmem_st16(tmem_addr(tmem, qd, C_DP + ch * 96 + c * 16), dk);
       }
@@ -464,6 +482,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       uint8_t* stage = sm + Q_OFF;
       const int src = ch == 0 ? C_DK : C_DV;
+      const float f = ch == 0 ? p.scale : 1.f;   // dK accumulated dS^T / scale
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         uint32_t u[32];
@@ -473,19 +492,21 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           uint4 w;
-          w.x = pack_bf16(__uint_as_float(u[8 * g]), __uint_as_float(u[8 * g + 1]));
-          w.y = pack_bf16(__uint_as_float(u[8 * g + 2]), __uint_as_float(u[8 * g + 3]));
-          w.z = pack_bf16(__uint_as_float(u[8 * g + 4]), __uint_as_float(u[8 * g + 5]));
-          w.w = pack_bf16(__uint_as_float(u[8 * g + 6]), __uint_as_float(u[8 * g + 7]));
+          w.x = pack_bf16(f * __uint_as_float(u[8 * g]), f * __uint_as_float(u[8 * g + 1]));
+          w.y = pack_bf16(f * __uint_as_float(u[8 * g + 2]), f * __uint_as_float(u[8 * g + 3]));
+          w.z = pack_bf16(f * __uint_as_float(u[8 * g + 4]), f * __uint_as_float(u[8 * g + 5]));
+          w.w = pack_bf16(f * __uint_as_float(u[8 * g + 6]), f * __uint_as_float(u[8 * g + 7]));
           *reinterpret_cast<uint4*>(box + (((k0 + g) ^ (r & 7)) << 4)) = w;
         }
       }
       {
         uint8_t* box = stage + (4 + ch) * BOX + r * 128;
+        const float sc = p.scale;
 #pragma unroll
         for (int g = 0; g < 8; ++g)
           *reinterpret_cast<float4*>(box + ((g ^ (r & 7)) << 4)) =
-              make_float4(acc[4 * g], acc[4 * g + 1], acc[4 * g + 2], acc[4 * g + 3]);
+              make_float4(sc * acc[4 * g], sc * acc[4 * g + 1], sc * acc[4 * g + 2],
+                          sc * acc[4 * g + 3]);
       }
       fence_proxy_async_smem();
       stored = true;
