@@ -47,6 +47,10 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, help="workload configuration (default 2)")
     ap.add_argument("--form", default="laga", choices=["laga", "explicit", "laga_fused"])
+    ap.add_argument("--no-block-variant", action="store_true",
+                    help="skip the timing of the full attention block beside the main line")
+    ap.add_argument("--block-d-model", type=int, default=7168,
+                    help="hidden size of the attention block variant (DeepSeek-V3: 7168)")
     ap.add_argument("--no-fused-variant", action="store_true",
                     help="skip the timing of the fused up-projection form beside the main line")
     ap.add_argument("--e2e-steps", type=int, default=10)
@@ -450,6 +454,9 @@ def run_ours(args, rank, world, local_rank):
     fused = None
     if args.form == "laga" and not args.no_fused_variant:
         fused = fused_variant(args, wl, t, dev, stream, flush, peak_tf)
+    block = None
+    if args.form == "laga" and not args.no_block_variant:
+        block = block_variant(args, wl, dev, stream, flush)
     attn_ms = sum(prof[k][0] for k in prof if k.startswith("attn")) / args.steps
     up_f = 3 * 2.0 * B * S * 512 * H * 256
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -474,7 +481,7 @@ def run_ours(args, rank, world, local_rank):
             "e2e": e2e,
             "gpu_launches": launches[0] * args.steps,
             "roofline": roof, "kernels": kernels, "cpu_baseline": cpu_baseline,
-            "fused_upproj_variant": fused}
+            "fused_upproj_variant": fused, "attention_block_variant": block}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -529,6 +536,50 @@ def fused_variant(args, wl, t, dev, stream, flush, peak_tf):
             "dkdv_fused_frac": round(units / (per * 1e-3) / 1e12 / peak_tf, 4),
             "saved_bytes": run.saved_bytes, "saved_bytes_laga": pkg._lib.workspace_bytes(base_dims, pkg._lib.WS_SAVED),
             "fwd_scratch_bytes": run.fwd_bytes}
+
+
+def block_variant(args, wl, dev, stream, flush):
+    """The full attention block (W_q, W_kv_a, the library's LAGA compute,
+    W_o; forward + backward) around the same shard: one rank's block holds
+    the shard's heads over the whole sequence, i.e. the per-rank work of a
+    sequence-parallel layer with P * H heads at degree P for the three
+    projections' head-wise GEMMs.  Returns its step time, tokens/s and the
+    rate of all its FLOPs."""
+    import torch
+    import sequence_latent_norm_gb300 as pkg
+    from laga_inputs import make_block_inputs
+    from sequence_latent_norm_gb300.block import LagaAttentionBlock
+    S, H, B, d = wl.S, wl.H, wl.B, args.block_d_model
+    t = {k: v.to(dev) for k, v in make_block_inputs(wl, d).items()}
+    blk = LagaAttentionBlock.single(H, S, B=B, device=dev)
+
+    def step():
+        blk.forward(t["h"], t["w_q"], t["w_kva"], t["gamma"], t["w_kvb"], t["w_o"], t["cos"],
+                    t["sin"])
+        blk.backward(t["dy"])
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    pkg._lib.sync_check()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    fwd_f, bwd_f = attention_flops(S, H, B)
+    # W_q, W_kv_a and W_o: one GEMM per weight forward, two backward
+    proj = 3 * 2.0 * B * S * d * (H * 192 + 576 + H * 128)
+    up = 3 * 2.0 * B * S * 512 * H * 256
+    return {"workload": f"MLA attention block, {H} heads, S={S}, d_model={d}, B={B}",
+            "ms_per_step": round(ms, 4), "tokens_per_s": round(B * S / (ms * 1e-3), 1),
+            "tflops_all_gemms_and_attention": round((fwd_f + bwd_f + proj + up) / (ms * 1e-3) / 1e12,
+                                                    2),
+            "projections": "W_q, W_kv_a, W_o as torch matmuls (cuBLAS), bf16 in and out"}
 
 
 # ----------------------------------------------------------------- sweep

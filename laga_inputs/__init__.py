@@ -96,3 +96,28 @@ def make_inputs(wl: Workload, with_grad_out: bool = True):
 def as_f64(t: torch.Tensor):
     """The exact values of a tensor as a float64 NumPy array."""
     return t.detach().to("cpu", torch.float64).numpy()
+
+
+def make_block_inputs(wl: Workload, d_model: int):
+    """Draw the inputs of the attention block around one workload (all heads
+    at one rank: n_h = wl.H): h [B, S, d_model] ~ N(0, 1); W_q [d_model,
+    n_h (d_nope + d_rope)] and W_kv_a [d_model, d_kv + d_rope] ~ N(0,
+    1/d_model), so that q and c keep the workload's unit variance; W_kv_b and
+    gamma as ``make_inputs``; W_o [n_h d_v, d_model] ~ N(0, 1/(n_h d_v));
+    dy [B, S, d_model] ~ N(0, 1).  Matrices in the I/O dtype, gamma and the
+    RoPE tables fp32, all on the CPU."""
+    g = torch.Generator(device="cpu").manual_seed(wl.seed + 7919)
+    dt = wl.torch_dtype
+    n_h = wl.H
+    h = torch.randn(wl.B, wl.S, d_model, generator=g)
+    w_q = torch.randn(d_model, n_h * wl.d_qk, generator=g) / math.sqrt(d_model)
+    w_kva = torch.randn(d_model, wl.d_kv + wl.d_rope, generator=g) / math.sqrt(d_model)
+    w_kvb = torch.randn(wl.d_kv, n_h * (wl.d_nope + wl.d_v), generator=g) / math.sqrt(wl.d_kv)
+    gamma = 1.0 + 0.1 * torch.randn(wl.d_kv, generator=g)
+    w_o = torch.randn(n_h * wl.d_v, d_model, generator=g) / math.sqrt(n_h * wl.d_v)
+    dy = torch.randn(wl.B, wl.S, d_model, generator=g)
+    out = {k: v.to(dt).contiguous() for k, v in
+           dict(h=h, w_q=w_q, w_kva=w_kva, w_kvb=w_kvb, w_o=w_o, dy=dy).items()}
+    out["gamma"] = gamma.float().contiguous()
+    out["cos"], out["sin"] = rope_tables(wl.S, wl.d_rope, wl.theta)
+    return out

@@ -38,6 +38,12 @@ Parity status per function (what pins it lives in ``tests/test_oracle.py``):
                            ratios printed in Section 4.2.
 * ``activation_elems``     pinned: the n_h*d_kv versus H*(d_nope+d_v)
                            per-token ratio stated in Sections 1, 3.2, 3.3.
+* ``block.block_forward`` /
+  ``block.block_backward`` the attention block of Algorithm 1 (W_q, W_kv_a,
+                           the per-rank compute, W_o) at one rank; pinned
+                           by central finite differences and by selection-
+                           matrix projections reducing it to ``forward`` /
+                           ``backward`` (tests/test_oracle_block.py).
 """
 
 from .laga import (  # noqa: F401

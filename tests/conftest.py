@@ -49,6 +49,9 @@ def pytest_terminal_summary(terminalreporter, exitstatus, config):
         g = {k: v for k, v in r.items() if k in ("dq", "dc", "dw", "dgamma")}
         if g:
             tr.write_line(f"{w}: gradients rel-fro " + ", ".join(f"{k} {v:.2e}" for k, v in g.items()))
+    for w, r in RECORDS:
+        if "block" in r:
+            tr.write_line(f"{w}: rel-fro " + ", ".join(f"{k} {v:.2e}" for k, v in r["block"].items()))
     grads = {}
     for w, r in RECORDS:
         for k, v in r.items():

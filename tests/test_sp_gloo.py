@@ -118,3 +118,54 @@ def test_sequence_parallel_comm_at_deepseek_v3_dims_matches_table1_form():
     (which is linear in S, so equality here is equality at S = 4K-16K)."""
     dims = dict(d_nope=128, d_rope=64, d_v=128, d_kv=512)
     mp.spawn(_rank, args=(2, _free_port(), 2, 8, dims, "layer"), nprocs=2, join=True)
+
+
+def _rank_block(rank, world, port, n_h, S, dims, d_model):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from oracle.block import block_backward, block_forward
+        from sequence_latent_norm_gb300.block import LagaAttentionBlock
+        from sequence_latent_norm_gb300.sp import SequenceParallelLaga
+        rng = np.random.default_rng(11)
+        qk, hkv = dims["d_nope"] + dims["d_rope"], dims["d_nope"] + dims["d_v"]
+        h = rng.standard_normal((1, S, d_model))
+        w_q = rng.standard_normal((d_model, n_h * qk)) / math.sqrt(d_model)
+        w_kva = rng.standard_normal((d_model, dims["d_kv"] + dims["d_rope"])) / math.sqrt(d_model)
+        gamma = 1.0 + 0.1 * rng.standard_normal(dims["d_kv"])
+        w_kvb = rng.standard_normal((dims["d_kv"], n_h * hkv)) / math.sqrt(dims["d_kv"])
+        w_o = rng.standard_normal((n_h * dims["d_v"], d_model)) / math.sqrt(n_h * dims["d_v"])
+        cos, sin = oracle.rope_tables(S, dims["d_rope"])
+        dy = rng.standard_normal((1, S, d_model))
+        full = oracle.Dims(S=S, H=n_h, **dims)
+        y, st = block_forward(h, w_q, w_kva, gamma, w_kvb, w_o, cos, sin, full)
+        g = block_backward(st, dy)
+        P, H, Sr = world, n_h // world, S // world
+        mine = oracle.Dims(S=S, H=H, n_h_total=n_h, head_offset=rank * H, **dims)
+        sp = SequenceParallelLaga(n_h, S, compute=OracleCompute(mine), **dims)
+        blk = LagaAttentionBlock(sp, n_h, distributed=True)
+        seq = slice(rank * Sr, (rank + 1) * Sr)
+        T = torch.from_numpy
+        y_loc = blk.forward(T(h[:, seq]).contiguous(), T(w_q), T(w_kva), T(gamma), T(w_kvb),
+                            T(w_o), T(cos), T(sin))
+        got = blk.backward(T(dy[:, seq]).contiguous())
+        tol = dict(rtol=1e-11, atol=1e-11)
+        np.testing.assert_allclose(y_loc.numpy(), y[:, seq], **tol)
+        np.testing.assert_allclose(got["dh"].numpy(), g["dh"][:, seq], **tol)
+        for k in ("dw_q", "dw_kva", "dw_o", "dw_kvb", "dgamma"):
+            np.testing.assert_allclose(got[k].numpy(), g[k], **tol, err_msg=k)
+        # the three replicated weights' gradients are all-reduced: ring bytes
+        # 2 (P-1)/P of each fp64 gradient
+        for k, w in (("dw_q", w_q), ("dw_kva", w_kva), ("dw_o", w_o)):
+            assert blk.sent["all_reduce_" + k] == 2 * (P - 1) * w.size * 8 // P
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("world,n_h,S", [(2, 4, 12), (4, 4, 8)])
+def test_sequence_parallel_attention_block_matches_unsharded_block_oracle(world, n_h, S):
+    """The whole block of Algorithm 1 (W_q, W_kv_a, the exchanges around the
+    per-rank compute, W_o) on CPU ranks equals the unsharded block oracle:
+    y and dh per sequence chunk, and the summed weight gradients."""
+    mp.spawn(_rank_block, args=(world, _free_port(), n_h, S, SMALL, 7), nprocs=world, join=True)
