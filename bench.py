@@ -452,10 +452,10 @@ def run_ours(args, rank, world, local_rank):
                 "peak_source": f"{peak_src} HBM copy"}
     roof["traffic"] = ncu_traffic(top, base.name)
     fused = None
-    if args.form == "laga" and not args.no_fused_variant:
+    if args.form == "laga" and world == 1 and not args.no_fused_variant:
         fused = fused_variant(args, wl, t, dev, stream, flush, peak_tf)
     block = None
-    if args.form == "laga" and not args.no_block_variant:
+    if args.form == "laga" and world == 1 and not args.no_block_variant:
         block = block_variant(args, wl, dev, stream, flush)
     attn_ms = sum(prof[k][0] for k in prof if k.startswith("attn")) / args.steps
     up_f = 3 * 2.0 * B * S * 512 * H * 256
