@@ -156,15 +156,18 @@ def test_laga_equals_explicit_form_bitwise_on_ragged_batch():
     check_grads(a, ref, where="ragged laga")
 
 
-def test_bwd_overlap_entry_point_is_bitwise_equal_to_laga_bwd():
+@pytest.mark.parametrize("form", ["laga", "laga_fused"])
+def test_bwd_overlap_entry_point_is_bitwise_equal_to_laga_bwd(form):
     """laga_bwd_overlap (the dQ kernel on a second stream of the caller's)
     computes exactly what laga_bwd does on one stream, and orders its work
-    before what follows on the compute stream."""
+    before what follows on the compute stream.  The fused form's dQ kernel
+    reads the K/V its dK/dV kernel rebuilds, so there the call keeps stream
+    order; the results are the same."""
     import sequence_latent_norm_gb300 as pkg
     wl = config(1, S=1000, H=4)
     dev = torch.device("cuda:0")
     t = {k: v.to(dev) for k, v in make_inputs(wl).items()}
-    run = pkg.Laga(shard_of(wl), device=dev)
+    run = pkg.Laga(shard_of(wl, form), device=dev)
     o, lse = run.forward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"])
     a = run.backward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"], o, lse, t["dO"])
     a = [x.clone() for x in a]
