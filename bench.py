@@ -451,12 +451,17 @@ def run_ours(args, rank, world, local_rank):
                 "unit": "GB/s", "frac": round(ach / peak_gbs, 4),
                 "peak_source": f"{peak_src} HBM copy"}
     roof["traffic"] = ncu_traffic(top, base.name)
+    # the variants run on the same inputs with the main line's workspaces
+    # and outputs released, so that each is timed in the memory state it
+    # would have alone
+    del run, o, lse, dq, dc, dw, dg
+    torch.cuda.empty_cache()
     fused = None
     if args.form == "laga" and world == 1 and not args.no_fused_variant:
-        fused = fused_variant(args, wl, t, dev, stream, flush, peak_tf)
+        fused = fused_variant(args, wl, t, dev, stream, flush, peak_tf, gpu_id)
     block = None
     if args.form == "laga" and world == 1 and not args.no_block_variant:
-        block = block_variant(args, wl, dev, stream, flush)
+        block = block_variant(args, wl, dev, stream, flush, gpu_id)
     attn_ms = sum(prof[k][0] for k in prof if k.startswith("attn")) / args.steps
     up_f = 3 * 2.0 * B * S * 512 * H * 256
     line = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
@@ -486,7 +491,7 @@ def run_ours(args, rank, world, local_rank):
         print(json.dumps(line), flush=True)
 
 
-def fused_variant(args, wl, t, dev, stream, flush, peak_tf):
+def fused_variant(args, wl, t, dev, stream, flush, peak_tf, gpu_id=None):
     """The fused up-projection form on the same inputs: step time (fwd +
     bwd, one stream), its dK/dV kernel's rate and the saved-activation
     bytes of both forms."""
@@ -503,6 +508,9 @@ def fused_variant(args, wl, t, dev, stream, flush, peak_tf):
         o, lse = run.forward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"])
         run.backward(t["q"], t["c"], t["w"], t["gamma"], t["cos"], t["sin"], o, lse, t["dO"])
 
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -525,6 +533,7 @@ def fused_variant(args, wl, t, dev, stream, flush, peak_tf):
     pkg._lib.profile_enable(False)
     prof = pkg._lib.profile_read()
     pkg._lib.sync_check()
+    clk = clocks.stop()
     k = "attn_bwd_dkdv_fused"
     per = prof[k][0] / prof[k][1]
     _, units = kernel_work(k, S, H, B)
@@ -535,10 +544,10 @@ def fused_variant(args, wl, t, dev, stream, flush, peak_tf):
             "dkdv_fused_tflops": round(units / (per * 1e-3) / 1e12, 2),
             "dkdv_fused_frac": round(units / (per * 1e-3) / 1e12 / peak_tf, 4),
             "saved_bytes": run.saved_bytes, "saved_bytes_laga": pkg._lib.workspace_bytes(base_dims, pkg._lib.WS_SAVED),
-            "fwd_scratch_bytes": run.fwd_bytes}
+            "fwd_scratch_bytes": run.fwd_bytes, "clocks": clk}
 
 
-def block_variant(args, wl, dev, stream, flush):
+def block_variant(args, wl, dev, stream, flush, gpu_id=None):
     """The full attention block (W_q, W_kv_a, the library's LAGA compute,
     W_o; forward + backward) around the same shard: one rank's block holds
     the shard's heads over the whole sequence, i.e. the per-rank work of a
@@ -558,6 +567,9 @@ def block_variant(args, wl, dev, stream, flush):
                     t["sin"])
         blk.backward(t["dy"])
 
+    clocks = ClockSampler(gpu_id)
+    clocks.start()
+    time.sleep(0.3)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -570,6 +582,7 @@ def block_variant(args, wl, dev, stream, flush):
         ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     pkg._lib.sync_check()
+    clk = clocks.stop()
     ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
     fwd_f, bwd_f = attention_flops(S, H, B)
     # W_q, W_kv_a and W_o: one GEMM per weight forward, two backward
@@ -579,7 +592,8 @@ def block_variant(args, wl, dev, stream, flush):
             "ms_per_step": round(ms, 4), "tokens_per_s": round(B * S / (ms * 1e-3), 1),
             "tflops_all_gemms_and_attention": round((fwd_f + bwd_f + proj + up) / (ms * 1e-3) / 1e12,
                                                     2),
-            "projections": "W_q, W_kv_a, W_o as torch matmuls (cuBLAS), bf16 in and out"}
+            "projections": "W_q, W_kv_a, W_o as torch matmuls (cuBLAS), bf16 in and out",
+            "clocks": clk}
 
 
 # ----------------------------------------------------------------- sweep
