@@ -7,25 +7,26 @@
 // CTAs, so every output element is one fixed-order accumulation.
 //
 // One CTA per (128-key tile j, head h, batch b), longest (smallest j)
-// first; it walks the query tiles i = j .. last.  12 warps:
-//   warps 0-7  compute.  Warp w owns TMEM lane quadrant w%4 (key rows) and
-//              column half w/4 (query columns).  Phase A: S^T -> P^T (bf16
-//              packed into its own S^T columns, the TMEM operand of dV).
-//              Phase B: dP^T -> dS^T / scale (bf16 packed into its own
-//              dP^T columns, the TMEM operand of dK; dK is scaled in the
-//              epilogue).  Then it adds this tile's
-//              k_pe part of dK from TMEM into registers.
-//   warp 8     TMA producer: K_j, V_j once; per i: Q_i with LSE_i and
+// first; it walks the query tiles i = j .. last.  20 warps:
+//   warps 0-15 compute.  Warp w owns TMEM lane quadrant w%4 (32 key rows)
+//              and column group g = w/4: query columns [16g, 16g+16) and
+//              [64+16g, 64+16g+16).  Phase A: S^T -> P^T (bf16 pairs packed
+//              into the first 64 S^T columns, the TMEM operand of dV).
+//              Phase B: dP^T -> dS^T / scale (packed into the first 64 dP^T
+//              columns, the TMEM operand of dK; dK is scaled in the
+//              epilogue).  Then it adds this tile's k_pe part of dK from
+//              TMEM into registers.  Four warps per SMSP hide the latency of
+//              the phases' TMEM and shared-memory loads.
+//   warp 16    TMA producer: K_j, V_j once; per i: Q_i with LSE_i and
 //              delta_i (double-buffered), dO_i.
-//   warp 9     TMEM allocator and MMA issuer.  Per i: dP^T_i, dV, the
+//   warp 17    TMEM allocator and MMA issuer.  Per i: dP^T_i, dV, the
 //              k_nope steps of S^T_{i+1} (overlapping phase B), the k_pe
 //              part of dK, the k_pe steps of S^T_{i+1}, dK_nope.
-//   warps 10-11 idle (they complete warpgroup 2 for the register split).
+//   warps 18-19 idle (they complete warpgroup 4 for the register split).
 // TMEM columns: dV [0,128), dK_nope [128,256), S^T [256,384) with P^T in
-// [256,288) and [352,384), dP^T [384,512) with dS^T in [384,416) and
-// [480,512); the k_pe part of dK for tile i goes to [416,480), the dP^T
-// columns phase B has read and left free.  Every mbarrier is waited phase
-// by phase, so parity waits are exact.
+// [256,320), dP^T [384,512) with dS^T in [384,448); the k_pe part of dK
+// for tile i goes to [448,512), the dP^T columns phase B has read and left
+// free.  Every mbarrier is waited phase by phase, so parity waits are exact.
 //
 // Fused form (the up-projection fused into the attention backward, the
 // LAGA page's Section 4.7 and Section 8 future work): instead of loading
@@ -56,10 +57,11 @@ constexpr int Q_OFF = 5 * BOX;           // Q_i: two buffers of 3 boxes
 constexpr int DO_OFF = 11 * BOX;         // dO_i: 2 boxes
 constexpr int LD_OFF = 13 * BOX;         // 2 x (LSE 512 B + delta 512 B)
 constexpr int SMEM_BYTES = LD_OFF + 2048 + 1024;   // + slack to align the base
-constexpr int THREADS = 384;   // 12 warps: 3 whole warpgroups for setmaxnreg
-constexpr int N_COMPUTE = 8;
+constexpr int THREADS = 640;   // 20 warps: 5 whole warpgroups for setmaxnreg
+constexpr int N_COMPUTE = 16;
+constexpr int W_PROD = 16, W_MMA = 17;  // warps 18-19 complete warpgroup 4
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int C_DV = 0, C_DK = 128, C_S = 256, C_DP = 384, C_DKR = C_DP + 32;
+constexpr int C_DV = 0, C_DK = 128, C_S = 256, C_DP = 384, C_DKR = C_DP + 64;
 constexpr uint32_t KV_BYTES = 5 * BOX;
 constexpr uint32_t Q_BYTES = 3 * BOX + 1024;    // Q_i + LSE_i + delta_i
 constexpr uint32_t DO_BYTES = 2 * BOX;
@@ -92,14 +94,34 @@ struct KvParams {
   int* err;
 };
 
-// Both packed tiles use the same layout: the 16 bf16 pairs of query
-// columns [32c, 32c+32) of half h land at base + 96h + 16c, so half 0 fills
-// [base, base+32) and half 1 [base+96, base+128).  Half 0 walks its chunks
-// c = 0, 1 and half 1 walks c = 1, 0; each write then lands on columns its
-// own warp has already read, and [base+32, base+96) is left free.
+// Column group g of the compute warps owns query columns [16g, 16g+16)
+// (piece 0) and [64+16g, 64+16g+16) (piece 1).  Both packed tiles use the
+// same layout: the 8 bf16 pairs of piece p of group g land at base + 16g +
+// 8p, inside columns the group's own warp read with piece 0, so the packed
+// tile fills [base, base+64) and [base+64, base+128) is left free.
 // TMEM column of the K-step s (16 query columns) of a packed tile:
 LAGA_DEVINL uint32_t packed_col(int base, int s) {
-  return s < 4 ? base + 8 * s : base + 96 + 8 * (s - 4);
+  return s < 4 ? base + 16 * s : base + 16 * (s - 4) + 8;
+}
+
+// 64 columns of an fp32 TMEM tile (this thread's row r, lane quadrant qd),
+// times f, as bf16 into one 64-column 128-byte swizzled box.
+LAGA_DEVINL void stage64(uint32_t tmem, int qd, int r, int col, float f, uint8_t* box) {
+  uint8_t* row = box + r * 128;
+#pragma unroll 1
+  for (int c = 0; c < 2; ++c) {
+    uint32_t u[32];
+    tmem_ld32(tmem_addr(tmem, qd, col + 32 * c), u);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 w;
+      w.x = pack_bf16(f * __uint_as_float(u[8 * k]), f * __uint_as_float(u[8 * k + 1]));
+      w.y = pack_bf16(f * __uint_as_float(u[8 * k + 2]), f * __uint_as_float(u[8 * k + 3]));
+      w.z = pack_bf16(f * __uint_as_float(u[8 * k + 4]), f * __uint_as_float(u[8 * k + 5]));
+      w.w = pack_bf16(f * __uint_as_float(u[8 * k + 6]), f * __uint_as_float(u[8 * k + 7]));
+      *reinterpret_cast<uint4*>(row + (((4 * c + k) ^ (r & 7)) << 4)) = w;
+    }
+  }
 }
 
 template <bool FUSED>
@@ -137,7 +159,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     mbar_init(&bar_kvready, N_COMPUTE);
     fence_barrier_init();
   }
-  if (warp == 9) {
+  if (warp == W_MMA) {
     tmem_alloc(&tmem_sh, TMEM_COLS);
     tmem_relinquish();
   }
@@ -152,15 +174,12 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int b = (int)(blockIdx.x % per) / p.H;
   const int k0 = j * BT;
   const int n_i = p.n_t - j;              // query tiles j .. n_t-1
-  // 168 registers a thread at launch (10 warps): warps 8-9 give back 112
-  // each, the compute warps take 24 each, 8*32*192 + 2*32*56 <= 320*168
-
-  // 168 registers a thread at launch (12 warps).  Warpgroup 2 (producer,
-  // MMA issuer, two idle warps) drops to 72, the compute warps rise to 200:
-  // 8*32*200 + 4*32*72 = 60416 <= 384*168, and 200+200+72 per SMSP.
-  if (warp >= 8) {
-  reg_shrink<72>();
-  if (warp == 8) {
+  // 96 registers a thread at launch (20 warps).  Warpgroup 4 (producer,
+  // MMA issuer, two idle warps) drops to 64, the four compute warpgroups
+  // rise to 104: 128 * (4 * 104 + 64) = 61440 <= 640 * 96.
+  if (warp >= W_PROD) {
+  reg_shrink<64>();
+  if (warp == W_PROD) {
     // ------------------------------------------------------------- producer
     if (lane == 0) {
       bool ok = true;
@@ -229,7 +248,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       if (FUSED) bulk_wait0();
     }
-  } else if (warp == 9) {
+  } else if (warp == W_MMA) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t idST = idesc_bf16(128, 128, 0, 0);
@@ -334,40 +353,25 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   }
   } else {
-  reg_grow<200>();
-    // ------------------------------------------------------------- compute warps 0..7
+    reg_grow<104>();
+    // ------------------------------------------------------------- compute warps 0..15
     const int qd = warp & 3;            // TMEM lane quadrant
-    const int ch = warp >> 2;           // column half
+    const int g = warp >> 2;            // column group (see packed_col)
     const int r = qd * 32 + lane;       // TMEM lane: key row
     const int key = k0 + r;
     const bool key_ok = key < p.S;
-    float acc[32];                      // this thread's 32 columns of the k_pe part of dK
+    float acc[16];                      // this thread's 16 columns of the k_pe part of dK
 #pragma unroll
-    for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+    for (int k = 0; k < 16; ++k) acc[k] = 0.f;
     bool live = true;
     if (FUSED) {
-      // the rebuilt k_nope_j (half 0) or v_j (half 1) rows, rounded to
-      // bf16, into the 128-byte swizzled K_j / V_j boxes
+      // the rebuilt k_nope_j (groups 0-1) or v_j (groups 2-3) rows, 64
+      // columns a group, rounded to bf16 into the K_j / V_j boxes
       live = mbar_wait(&bar_kvacc, 0, p.err);
       if (live) {
         tc_fence_after();
-        uint8_t* dst = sm + (ch == 0 ? K_OFF : V_OFF);
-#pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t u[32];
-          tmem_ld32(tmem_addr(tmem, qd, C_S + ch * 128 + cc * 32), u);
-          uint8_t* row = dst + (cc >> 1) * BOX + r * 128;
-          const int g0 = (cc & 1) * 4;
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            uint4 w;
-            w.x = pack_bf16(__uint_as_float(u[8 * g]), __uint_as_float(u[8 * g + 1]));
-            w.y = pack_bf16(__uint_as_float(u[8 * g + 2]), __uint_as_float(u[8 * g + 3]));
-            w.z = pack_bf16(__uint_as_float(u[8 * g + 4]), __uint_as_float(u[8 * g + 5]));
-            w.w = pack_bf16(__uint_as_float(u[8 * g + 6]), __uint_as_float(u[8 * g + 7]));
-            *reinterpret_cast<uint4*>(row + (((g0 + g) ^ (r & 7)) << 4)) = w;
-          }
-        }
+        stage64(tmem, qd, r, C_S + 64 * g, 1.f,
+                sm + (g < 2 ? K_OFF + g * BOX : V_OFF + (g - 2) * BOX));
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -384,130 +388,105 @@ __global__ void __launch_bounds__(THREADS, 1)
       if (!mbar_wait(&bar_q_full[t & 1], (t >> 1) & 1, p.err)) break;   // LSE_i, delta_i
       if (!mbar_wait(&bar_s, t & 1, p.err)) break;
       tc_fence_after();
-      float pv[64];
+      float pv[32];
       // query tiles after the diagonal that end inside the sequence need no mask
       const bool full = t > 0 && q0 + BT <= p.S && k0 + BT <= p.S;
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int c = kk ^ ch;          // chunk of this pass (see packed_col)
-        const int col0 = ch * 64 + c * 32;
-        uint32_t us[32];
-        tmem_ld32(tmem_addr(tmem, qd, C_S + col0), us);
-        const float4* l4 = reinterpret_cast<const float4*>(lse_s + col0);
+      for (int pc = 0; pc < 2; ++pc) {
+        const int col0 = 64 * pc + 16 * g;
+        uint32_t us[16];
+        tmem_ld16(tmem_addr(tmem, qd, C_S + col0), us);
         if (full) {
-          // all of the chunk's LSE values first: shared-memory loads wait
-          // behind the tensor core's operand reads, so none may sit between
-          // the exponentials
-          float4 lz[8];
+          // the piece's LSE values first: shared-memory loads wait behind
+          // the tensor core's operand reads, so none may sit between the
+          // exponentials
+          const float4* l4 = reinterpret_cast<const float4*>(lse_s + col0);
+          float4 lz[4];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) lz[k] = l4[k];
+          for (int k = 0; k < 4; ++k) lz[k] = l4[k];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float4 l = lz[k];
-            float* o = pv + kk * 32 + 4 * k;
-            const float x0 = fmaf(__uint_as_float(us[4 * k]), p.sl2, -l.x);
-            const float x1 = fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -l.y);
-            const float x2 = fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -l.z);
-            const float x3 = fmaf(__uint_as_float(us[4 * k + 3]), p.sl2, -l.w);
-            o[0] = ex2(x0); o[1] = ex2(x1); o[2] = ex2(x2); o[3] = ex2(x3);
+          for (int k = 0; k < 4; ++k) {
+            float* o = pv + 16 * pc + 4 * k;
+            o[0] = ex2(fmaf(__uint_as_float(us[4 * k]), p.sl2, -lz[k].x));
+            o[1] = ex2(fmaf(__uint_as_float(us[4 * k + 1]), p.sl2, -lz[k].y));
+            o[2] = ex2(fmaf(__uint_as_float(us[4 * k + 2]), p.sl2, -lz[k].z));
+            o[3] = ex2(fmaf(__uint_as_float(us[4 * k + 3]), p.sl2, -lz[k].w));
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
+          for (int k = 0; k < 16; ++k) {
             const int col = col0 + k;
             const bool ok = key_ok && col >= qlo && col < qhi;
-            pv[kk * 32 + k] =
-                ok ? ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[col])) : 0.f;
+            pv[16 * pc + k] = ok ? ex2(fmaf(__uint_as_float(us[k]), p.sl2, -lse_s[col])) : 0.f;
           }
         }
-        uint32_t pk[16];
+        uint32_t pk[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          pk[k] = pack_bf16(pv[kk * 32 + 2 * k], pv[kk * 32 + 2 * k + 1]);
-        tmem_st16(tmem_addr(tmem, qd, C_S + ch * 96 + c * 16), pk);
+        for (int k = 0; k < 8; ++k) pk[k] = pack_bf16(pv[16 * pc + 2 * k], pv[16 * pc + 2 * k + 1]);
+        tmem_st8(tmem_addr(tmem, qd, C_S + 16 * g + 8 * pc), pk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p);
       // ---- phase B: dS^T / scale = P^T (dP^T - delta), packed like P^T
-      //      into the ends of the dP^T columns (dK is scaled once, in the
-      //      epilogue)
+      //      into the first 64 dP^T columns (dK is scaled in the epilogue)
       if (!mbar_wait(&bar_dp, t & 1, p.err)) break;
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int c = kk ^ ch;
-        const int col0 = ch * 64 + c * 32;
-        uint32_t ud[32], dk[16];
-        tmem_ld32(tmem_addr(tmem, qd, C_DP + col0), ud);
-        // all of the chunk's delta values first (see phase A)
+      for (int pc = 0; pc < 2; ++pc) {
+        const int col0 = 64 * pc + 16 * g;
+        // the piece's delta values first (see phase A)
         const float4* d4 = reinterpret_cast<const float4*>(dlt_s + col0);
-        float4 dz[8];
+        float4 dz[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) dz[k] = d4[k];
+        for (int k = 0; k < 4; ++k) dz[k] = d4[k];
+        uint32_t ud[16], dk[8];
+        tmem_ld16(tmem_addr(tmem, qd, C_DP + col0), ud);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < 4; ++k) {
           const float4 dl = dz[k];
           const float* u = reinterpret_cast<const float*>(ud) + 4 * k;
-          const float* pk = pv + kk * 32 + 4 * k;
+          const float* pk = pv + 16 * pc + 4 * k;
           dk[2 * k] = pack_bf16(pk[0] * (u[0] - dl.x), pk[1] * (u[1] - dl.y));
           dk[2 * k + 1] = pack_bf16(pk[2] * (u[2] - dl.z), pk[3] * (u[3] - dl.w));
         }
-        tmem_st16(tmem_addr(tmem, qd, C_DP + ch * 96 + c * 16), dk);
+        tmem_st8(tmem_addr(tmem, qd, C_DP + 16 * g + 8 * pc), dk);
       }
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_ds);
-      // ---- the k_pe part of dK for this query tile, out of [416,480)
+      // ---- the k_pe part of dK for this query tile, out of [448,512)
       if (!mbar_wait(&bar_dkr, t & 1, p.err)) break;
       tc_fence_after();
       {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, qd, C_DKR + ch * 32), u);
+        uint32_t u[16];
+        tmem_ld16(tmem_addr(tmem, qd, C_DKR + 16 * g), u);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) acc[k] += __uint_as_float(u[k]);
+        for (int k = 0; k < 16; ++k) acc[k] += __uint_as_float(u[k]);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_tfree);
     }
-    // ---- epilogue: dK_nope (half 0) or dV (half 1) rows as bf16, and the
-    //      k_pe part of dK as fp32, staged in the idle Q buffers as 128-byte
-    //      swizzled boxes (four 64-column bf16 boxes, two 32-column fp32
-    //      boxes) and written by TMA after the final barrier; rows past the
-    //      sequence are clipped there
+    // ---- epilogue: dK_nope (groups 0-1, scaled) or dV (groups 2-3) rows as
+    //      bf16, 64 columns a group, and the k_pe part of dK, scaled, as
+    //      fp32; staged in the idle Q buffers as 128-byte swizzled boxes
+    //      (four 64-column bf16 boxes, two 32-column fp32 boxes) and written
+    //      by TMA after the final barrier; rows past the sequence are
+    //      clipped there
     if (mbar_wait(&bar_fin, 0, p.err)) {
       tc_fence_after();
-      uint8_t* stage = sm + Q_OFF;
-      const int src = ch == 0 ? C_DK : C_DV;
-      const float f = ch == 0 ? p.scale : 1.f;   // dK accumulated dS^T / scale
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(tmem_addr(tmem, qd, src + c * 32), u);
-        uint8_t* box = stage + (ch * 2 + (c >> 1)) * BOX + r * 128;
-        const int k0 = (c & 1) * 4;
+      stage64(tmem, qd, r, g < 2 ? C_DK + 64 * g : C_DV + 64 * (g - 2), g < 2 ? p.scale : 1.f,
+              sm + Q_OFF + g * BOX);
+      uint8_t* box = sm + Q_OFF + (4 + (g >> 1)) * BOX + r * 128;
+      const float sc = p.scale;
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          uint4 w;
-          w.x = pack_bf16(f * __uint_as_float(u[8 * g]), f * __uint_as_float(u[8 * g + 1]));
-          w.y = pack_bf16(f * __uint_as_float(u[8 * g + 2]), f * __uint_as_float(u[8 * g + 3]));
-          w.z = pack_bf16(f * __uint_as_float(u[8 * g + 4]), f * __uint_as_float(u[8 * g + 5]));
-          w.w = pack_bf16(f * __uint_as_float(u[8 * g + 6]), f * __uint_as_float(u[8 * g + 7]));
-          *reinterpret_cast<uint4*>(box + (((k0 + g) ^ (r & 7)) << 4)) = w;
-        }
-      }
-      {
-        uint8_t* box = stage + (4 + ch) * BOX + r * 128;
-        const float sc = p.scale;
-#pragma unroll
-        for (int g = 0; g < 8; ++g)
-          *reinterpret_cast<float4*>(box + ((g ^ (r & 7)) << 4)) =
-              make_float4(sc * acc[4 * g], sc * acc[4 * g + 1], sc * acc[4 * g + 2],
-                          sc * acc[4 * g + 3]);
-      }
+      for (int k = 0; k < 4; ++k)
+        *reinterpret_cast<float4*>(box + ((((g & 1) * 4 + k) ^ (r & 7)) << 4)) =
+            make_float4(sc * acc[4 * k], sc * acc[4 * k + 1], sc * acc[4 * k + 2],
+                        sc * acc[4 * k + 3]);
       fence_proxy_async_smem();
       stored = true;
     }
@@ -523,7 +502,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bulk_commit();
     bulk_wait_read0();
   }
-  if (warp == 9) {
+  if (warp == W_MMA) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }

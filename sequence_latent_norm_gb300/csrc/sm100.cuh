@@ -258,6 +258,26 @@ LAGA_DEVINL void tmem_ld64(uint32_t taddr, uint32_t (&r)[64]) {
       : "r"(taddr)
       : "memory");
 }
+// TMEM -> registers: this warp's 32 lanes, 16 consecutive 32-bit columns,
+// the load and its completion wait in one asm statement.
+LAGA_DEVINL void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+// registers -> TMEM: this warp's 32 lanes, 8 consecutive 32-bit columns.
+LAGA_DEVINL void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+      : "memory");
+}
 // registers -> TMEM: this warp's 32 lanes, 16 consecutive 32-bit columns.
 LAGA_DEVINL void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
