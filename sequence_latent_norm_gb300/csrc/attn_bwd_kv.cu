@@ -391,11 +391,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       float pv[32];
       // query tiles after the diagonal that end inside the sequence need no mask
       const bool full = t > 0 && q0 + BT <= p.S && k0 + BT <= p.S;
+      // both pieces' scores in one TMEM round trip
+      uint32_t usa[32];
+      tmem_ld16x2(tmem_addr(tmem, qd, C_S + 16 * g), tmem_addr(tmem, qd, C_S + 64 + 16 * g), usa);
 #pragma unroll
       for (int pc = 0; pc < 2; ++pc) {
         const int col0 = 64 * pc + 16 * g;
-        uint32_t us[16];
-        tmem_ld16(tmem_addr(tmem, qd, C_S + col0), us);
+        const uint32_t* us = usa + 16 * pc;
         if (full) {
           // the piece's LSE values first: shared-memory loads wait behind
           // the tensor core's operand reads, so none may sit between the
@@ -433,6 +435,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       //      into the first 64 dP^T columns (dK is scaled in the epilogue)
       if (!mbar_wait(&bar_dp, t & 1, p.err)) break;
       tc_fence_after();
+      uint32_t uda[32];
+      tmem_ld16x2(tmem_addr(tmem, qd, C_DP + 16 * g), tmem_addr(tmem, qd, C_DP + 64 + 16 * g), uda);
 #pragma unroll
       for (int pc = 0; pc < 2; ++pc) {
         const int col0 = 64 * pc + 16 * g;
@@ -441,8 +445,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         float4 dz[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) dz[k] = d4[k];
-        uint32_t ud[16], dk[8];
-        tmem_ld16(tmem_addr(tmem, qd, C_DP + col0), ud);
+        uint32_t dk[8];
+        const uint32_t* ud = uda + 16 * pc;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float4 dl = dz[k];
