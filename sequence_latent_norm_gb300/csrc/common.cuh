@@ -34,11 +34,6 @@ LAGA_DEVINL float warp_sum(float v) {
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
-LAGA_DEVINL float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
 
 // Layout of the per-head K/V tensor [.., 256]: element (b, s, h, e) sits at
 // b*sb + s*ss + h*sh + e.  Token-major (LAGA) and head-major (explicit form)
