@@ -32,19 +32,21 @@ def _run_block(blk, t):
     return y, g
 
 
+@pytest.mark.parametrize("form", ["laga", "laga_fused"])
 @pytest.mark.parametrize("case", [dict(S=640, H=4, d_model=384), dict(S=257, H=2, B=2, d_model=256)],
                          ids=["S640-H4", "S257-B2"])
-def test_attention_block_matches_block_oracle(case):
+def test_attention_block_matches_block_oracle(case, form):
     import sequence_latent_norm_gb300 as pkg
     from oracle import Dims
     from oracle.block import block_backward, block_forward
     from sequence_latent_norm_gb300.block import LagaAttentionBlock
+    case = dict(case)
     d_model = case.pop("d_model")
     wl = config(1, n_h_total=case["H"], **case)
     cpu = make_block_inputs(wl, d_model)
     dev = torch.device("cuda:0")
     t = {k: v.to(dev) for k, v in cpu.items()}
-    blk = LagaAttentionBlock.single(wl.H, wl.S, B=wl.B, device=dev)
+    blk = LagaAttentionBlock.single(wl.H, wl.S, B=wl.B, device=dev, form=form)
     y, g = _run_block(blk, t)
     pkg._lib.sync_check()
     a = {k: as_f64(v) for k, v in cpu.items()}
@@ -55,7 +57,7 @@ def test_attention_block_matches_block_oracle(case):
     errs = {"y": _rel_fro(as_f64(y), y_ref)}
     for k in ("dh", "dw_q", "dw_kva", "dw_o", "dw_kvb", "dgamma"):
         errs[k] = _rel_fro(as_f64(g[k]), ref[k])
-    RECORDS.append((f"block {wl.name} S={wl.S} H={wl.H} B={wl.B} d_model={d_model}",
+    RECORDS.append((f"block {form} S={wl.S} H={wl.H} B={wl.B} d_model={d_model}",
                     {"block": errs}))
     for k, e in errs.items():
         assert e <= BLOCK_REL_FRO, f"{k}: rel-fro {e:.3e}"
